@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Throughput of KV² compression on GB300: compressed context tokens/s over
+all layers, with the roofline fraction of the dominant kernel.
+
+One step = the whole hot path on one synthetic cache (Llama-3.1-8B shape,
+16K context by default): KeyDiff proxy -> per-chunk query selection ->
+tensor-core reconstruction scoring (row LSE pass + chunk column-max pass) ->
+sink pinning + eviction -> headwise compaction, through kvc_compress.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank compresses its own cache (independent problems, no
+collective on the data path); rank 0 prints one JSON line with the job-wide
+throughput (max time over ranks).  `--impl reference` times the float64 CPU
+oracle on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import kv_synth as ks  # noqa: E402
+
+METRIC = "compressed ctx tokens/s (all layers) at Llama-8B-shape 16K; % of roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=ks.LLAMA_16K.name, choices=list(ks.KV2_CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- workload arithmetic
+def plan_of(cfg):
+    """(chunk sizes, n_q per chunk) by the chunking rule of the KV² page."""
+    sizes, nqs = [], []
+    lo = cfg.sinks
+    while lo < cfg.N:
+        hi = min(lo + cfg.m, cfg.N)
+        sizes.append(hi - lo)
+        nqs.append(max(int(math.floor(cfg.rho * (hi - lo) + 1e-9)), 1))
+        lo = hi
+    return sizes, nqs
+
+
+def algorithmic_work(cfg):
+    """Per-step algorithmic FLOPs of the two scoring passes and bytes of the
+    bandwidth-bound stages (see the design notes)."""
+    sizes, nqs = plan_of(cfg)
+    d, L, Hq, Hkv, N = cfg.d, cfg.L, cfg.Hq, cfg.Hkv, cfg.N
+    Q = sum(nqs)
+    f_lse = L * Hq * 2 * d * sum(n * (N + (n + 1) / 2) for n in nqs)
+    f_col = L * Hq * 2 * d * sum(n * c for n, c in zip(nqs, sizes))
+    k = int(math.floor(cfg.budget * N + 1e-9))
+    b_k = L * Hkv * N * d * 2                       # one read of K
+    b = {
+        "keydiff": b_k + L * Hkv * N * 4,           # read K, write s
+        "recon_gather": L * Hq * Q * d * 2 * 2 + L * Hkv * Q * d * 2 * 2,
+        "evict_topk": L * Hkv * N * 4 + L * Hkv * k * 4,
+        "compact": 2 * 2 * L * Hkv * k * d * 2,     # read + write kept K and V
+    }
+    return {"flops_lse": f_lse * cfg.passes, "flops_colmax": f_col * cfg.passes, "Q": Q, "k": k,
+            "bytes": b, "flops_lse_per_launch": f_lse, "flops_colmax_per_launch": f_col}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        rows = [[c.strip() for c in r] for r in rows]
+        if self.uuid:
+            mine = [r for r in rows if r[0] == self.uuid]
+            rows = mine or rows
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+class OracleSample:
+    """Times the float64 oracle on a bounded sample of the workload and
+    scales it to one full step.  Sample units: the KeyDiff proxy and the
+    eviction of one (layer, KV head), the selection over all chunks, and the
+    reconstruction scoring of one (query head, chunk) -- the oracle's
+    per-head work is the same for every head, so a full step costs
+    L*Hkv*(proxy + evict) + L*Hq*M*(one scoring unit) + selection."""
+
+    def __init__(self, cfg):
+        from oracle import kv2
+        self.kv2 = kv2
+        self.cfg = cfg
+        dr = ks.gen_layer(cfg, 0, with_values=False)
+        self.K0 = kv2.bf16_to_f64(dr.K[0])
+        self.Q0 = kv2.bf16_to_f64(dr.Q[0])
+        self.s = kv2.keydiff_head(self.K0)
+        self.sel, self.chunks = kv2.select_queries(self.s, cfg.N, cfg.sinks, cfg.m, cfg.rho)
+        self.k = int(math.floor(cfg.budget * cfg.N + 1e-9))
+        self.unit = 0
+
+    def per_head(self):
+        kv2, cfg = self.kv2, self.cfg
+        a = time.perf_counter()
+        kv2.keydiff_head(self.K0)
+        sc = np.random.default_rng(0).random((1, 1, cfg.N))
+        kv2.evict(sc, cfg.sinks, [self.k])
+        b = time.perf_counter()
+        kv2.select_queries(self.s, cfg.N, cfg.sinks, cfg.m, cfg.rho)
+        c = time.perf_counter()
+        return b - a, c - b
+
+    def scoring_unit(self):
+        kv2 = self.kv2
+        c = self.chunks[self.unit % len(self.chunks)]
+        self.unit += 1
+        idx = self.sel[c.off:c.off + c.nq]
+        one = kv2.Chunk(c.lo, c.hi, 0, c.nq)
+        a = time.perf_counter()
+        kv2.recon_head(self.K0, self.Q0[idx][None], self.K0[idx], [one])
+        return time.perf_counter() - a
+
+    def full_step(self, t_head, t_sel, t_unit):
+        cfg = self.cfg
+        return cfg.passes * (cfg.L * cfg.Hkv * t_head + cfg.L * cfg.Hq * len(self.chunks) * t_unit + t_sel)
+
+    def describe(self, units):
+        cfg = self.cfg
+        return (f"oracle on {units} (query head, chunk) scoring unit(s) of {cfg.L * cfg.Hq * len(self.chunks)} "
+                f"plus KeyDiff+eviction of 1 of {cfg.L * cfg.Hkv} heads and the selection, "
+                f"{cfg.name}; scaled to the full step")
+
+
+def time_oracle_sample(cfg, budget_s=20.0, sampler=None):
+    """(seconds per full step, description): scoring units until `budget_s`
+    of CPU time (at least one)."""
+    smp = sampler or OracleSample(cfg)
+    t_head, t_sel = smp.per_head()
+    times = []
+    t0 = time.perf_counter()
+    while True:
+        times.append(smp.scoring_unit())
+        if time.perf_counter() - t0 >= budget_s or len(times) >= 64:
+            break
+    t_unit = statistics.median(times)
+    return smp.full_step(t_head, t_sel, t_unit), smp.describe(len(times))
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return
+    smp = OracleSample(cfg)
+    sample = []
+    for _ in range(args.warmup):
+        time_oracle_sample(cfg, budget_s=0.0, sampler=smp)
+    desc = ""
+    for _ in range(args.steps):
+        full, desc = time_oracle_sample(cfg, budget_s=0.0, sampler=smp)
+        sample.append(full)
+    t = statistics.median(sample)
+    value = cfg.N / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(cfg),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                         "sample": "per step: " + desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(cfg):
+    return {"workload": cfg.name, "L": cfg.L, "Hkv": cfg.Hkv, "Hq": cfg.Hq, "d": cfg.d, "N": cfg.N,
+            "sinks": cfg.sinks, "m": cfg.m, "rho": cfg.rho, "budget": cfg.budget, "passes": cfg.passes,
+            "needle_clusters_per_layer": cfg.needles_per_layer,
+            "l2": "inputs larger than L2 (K alone exceeds the 129 MB L2); no flush between steps",
+            "parallelism": "independent cache per GPU"}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import query_agnostic_kv_gb300 as qk
+    from query_agnostic_kv_gb300 import _build
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _build.build_library()
+    qk.kvc_device_check()
+    # each rank compresses its own cache
+    cfg_r = ks.scaled(cfg, seed=cfg.seed + rank)
+    x = ks.gen_kv2(cfg_r)
+    L, H, Hq, N, S, d = cfg.L, cfg.Hkv, cfg.Hq, cfg.N, cfg.sinks, cfg.d
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    K, V, Q = dev_bf16(x.K), dev_bf16(x.V), dev_bf16(x.Q)
+    shape = (L, H, Hq, d, N)
+    k = qk.kvc_budget_count(cfg.budget, N, S)
+    kl = [k] * L
+    ws = torch.empty(qk.kvc_workspace_size(shape, S, cfg.m, cfg.rho), dtype=torch.uint8, device=dev)
+    kept = torch.empty(L * H * k, dtype=torch.int32, device=dev)
+    Kc = torch.empty(L * H * k * d, dtype=torch.bfloat16, device=dev)
+    Vc = torch.empty_like(Kc)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qk.kvc_compress(shape, K, V, Q, S, cfg.m, cfg.rho, cfg.passes, kl, kept, Kc, Vc, ws=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = qk.kvc_stream_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {qk.kvc_status_string(st)}")
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.6)  # let the sampler take its first samples before the timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    qk.kvc_profile_begin()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = qk.kvc_profile_end()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    st = qk.kvc_stream_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {qk.kvc_status_string(st)}")
+    t_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    ms_per_step = t_max / args.steps
+    value = world * N * args.steps / (t_max / 1e3)
+
+    # ---- per-kernel breakdown and roofline of the dominant kernel
+    work = algorithmic_work(cfg)
+    peaks, peak_src = load_peaks()
+    launches = sum(v[0] for v in prof.values())
+    total_k = sum(v[1] for v in prof.values())
+    kernels = {n: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / total_k if total_k else None}
+               for n, v in prof.items()}
+    lse_avg_s = prof["recon_lse"][1] / prof["recon_lse"][0] / 1e3
+    col_avg_s = prof["recon_colmax"][1] / prof["recon_colmax"][0] / 1e3
+    peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    ach_lse = work["flops_lse_per_launch"] / lse_avg_s / 1e12
+    ach_col = work["flops_colmax_per_launch"] / col_avg_s / 1e12
+    roof = {"kernel": "recon_lse (tcgen05 row-LSE pass)", "bound": "tensor", "achieved": ach_lse,
+            "peak": peak_tf, "unit": "TFLOP/s", "frac": ach_lse / peak_tf, "traffic": None,
+            "peak_source": f"bf16_tflops_sustained of {peak_src} peaks",
+            "algorithmic_flops_per_launch": work["flops_lse_per_launch"]}
+    hbm = peaks.get("hbm_gbs")
+    bw = {}
+    for name, b in work["bytes"].items():
+        if name in prof:
+            avg = prof[name][1] / prof[name][0] / 1e3
+            bw[name] = {"GB/s": b / avg / 1e9, "frac_of_hbm": b / avg / 1e9 / hbm}
+    # whole-step roofline (slower of tensor FLOPs and HBM bytes)
+    f_all = work["flops_lse"] + work["flops_colmax"]
+    b_all = sum(work["bytes"].values())
+    t_roof = max(f_all / (peak_tf * 1e12), b_all / (hbm * 1e9))
+    step_roof = {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_per_step / 1e3),
+                 "tokens_per_s_at_roof": N / t_roof}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        hK = torch.from_numpy(x.K.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hV = torch.from_numpy(x.V.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hQ = torch.from_numpy(x.Q.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hkept = torch.empty(kept.shape, dtype=torch.int32).pin_memory()
+        hKc = torch.empty(Kc.shape, dtype=torch.bfloat16).pin_memory()
+        hVc = torch.empty(Vc.shape, dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            K.copy_(hK, non_blocking=True)
+            V.copy_(hV, non_blocking=True)
+            Q.copy_(hQ, non_blocking=True)
+            step()
+            hkept.copy_(kept, non_blocking=True)
+            hKc.copy_(Kc, non_blocking=True)
+            hVc.copy_(Vc, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = (hK.numel() + hV.numel() + hQ.numel()) * 2
+        d2h = hkept.numel() * 4 + (hKc.numel() + hVc.numel()) * 2
+        e2e = {"value": world * N * args.e2e_steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.e2e_steps}
+
+    # ---- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        full, desc = time_oracle_sample(cfg, budget_s=20.0)
+        cpu = {"value": N / full, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": desc,
+               "extrapolated_s_per_step": full}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(cfg),
+            "roofline": roof, "step_roofline": step_roof, "bandwidth": bw, "kernels": kernels,
+            "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    cfg = ks.KV2_CONFIGS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, cfg, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, cfg, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

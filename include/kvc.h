@@ -1,0 +1,260 @@
+/*
+ * kvc.h -- C ABI of the GB300 (sm_103a) attention-score KV-cache compressor.
+ *
+ * The method is KV^2 as described on "KV²가 전체 문맥 재계산 없이 KV 캐시를
+ * 압축한다" (onedev.kr/papers/598) and the block prefill of "[26'ICML] EpiCache"
+ * (juyoungkimmy-kim.github.io).  Each entry point below names the section it
+ * implements.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Types      bf16 tensors are passed as `const void*` (IEEE bfloat16 bit
+ *            patterns); scores are float32; indices are int32.
+ * Layout     row-major, contiguous, head dimension d innermost:
+ *              K, V      [L][Hkv][N][d]        cache keys / values (post-RoPE)
+ *              Qpool     [L][Hq][N][d]         one query per position and query head
+ *              p         [N]                   token-level proxy score
+ *              s         [L][Hkv][N]           per-head proxy score
+ *              score     [L][Hkv][N]           stage-2 (reconstruction) score
+ *              sel       [Q]                   selected positions, chunk-major, ascending inside a chunk
+ *              lse       [L][Hq][Q]            natural-log softmax normaliser of each reconstruction query
+ *              kept      ragged, layer-major:  layer l starts at Hkv * sum_{l'<l} k_{l'}, then [Hkv][k_l]
+ *              Kc, Vc    ragged like kept, d elements per row
+ *            Query head g reads KV head g / (Hq / Hkv).  d must be 128.
+ * Memory     The caller owns every buffer (device memory unless stated as
+ *            host), including the workspace; the library never allocates or
+ *            frees memory.  Pointers must be 16-byte aligned; the workspace
+ *            must be 256-byte aligned.
+ * Streams    All device work is enqueued on `stream` (NULL = legacy default
+ *            stream) and is asynchronous; host-side outputs are written
+ *            before the call returns.
+ * Errors     Argument errors are detected on the host before anything is
+ *            launched or written and return KVC_ERR_INVALID (or
+ *            KVC_ERR_WORKSPACE).  A failed launch or CUDA call returns
+ *            KVC_ERR_CUDA.  Device-side conditions (a bounded wait that
+ *            expired, an index that failed its check) are recorded in a
+ *            per-device status word and reported by kvc_stream_status().
+ *            On such an error the outputs are unspecified.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVC_API __attribute__((visibility("default")))
+#else
+#define KVC_API
+#endif
+
+typedef struct CUstream_st* kvc_stream; /* identical to cudaStream_t */
+
+typedef enum {
+  KVC_OK = 0,
+  KVC_ERR_INVALID = 1,     /* bad argument; nothing was launched or written */
+  KVC_ERR_CUDA = 2,        /* a CUDA runtime call or kernel launch failed */
+  KVC_ERR_TIMEOUT = 3,     /* a bounded device-side wait expired */
+  KVC_ERR_BOUNDS = 4,      /* a device-side index check failed */
+  KVC_ERR_WORKSPACE = 5,   /* workspace missing, misaligned or too small */
+  KVC_ERR_UNSUPPORTED = 6  /* current device is not an sm_103 GPU */
+} kvc_status;
+
+/* Model shape.  d must be 128, Hq a positive multiple of Hkv, N >= 1. */
+typedef struct {
+  int32_t L, Hkv, Hq, d, N;
+} kvc_shape;
+
+/* Human-readable name of a status code (static string). */
+KVC_API const char* kvc_status_string(kvc_status s);
+
+/* Checks that the current CUDA device is an sm_103 GPU this library was
+ * built for.  Returns KVC_OK, KVC_ERR_UNSUPPORTED or KVC_ERR_CUDA. */
+KVC_API kvc_status kvc_device_check(void);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device: KVC_OK, KVC_ERR_TIMEOUT or KVC_ERR_BOUNDS (or
+ * KVC_ERR_CUDA if the synchronisation itself failed). */
+KVC_API kvc_status kvc_stream_status(kvc_stream stream);
+
+/* Upper bound (ns) on every device-side wait of this library's kernels on
+ * the current process; 0 restores the default (1 s).  Host-only. */
+KVC_API kvc_status kvc_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Launches one block whose wait on a barrier that nothing completes must
+ * expire after `limit_ns`; the status word then reads KVC_ERR_TIMEOUT.
+ * This exercises the timeout path without hanging the GPU. */
+KVC_API kvc_status kvc_debug_expire_wait(uint64_t limit_ns, kvc_stream stream);
+
+/* Per-kernel timing.  Between kvc_profile_begin() and kvc_profile_end()
+ * every kernel this library launches is bracketed by a pair of CUDA events
+ * on its stream (reused from a pool; no device memory is allocated).
+ * kvc_profile_end() synchronises the device, fills up to `max_entries`
+ * records (one per kernel name, launches and summed milliseconds, in first-
+ * launch order) and sets *n_entries.  Profiling is process-wide and meant
+ * for one stream at a time. */
+typedef struct {
+  char name[32];
+  int32_t launches;
+  double total_ms;
+} kvc_kernel_time;
+KVC_API kvc_status kvc_profile_begin(void);
+KVC_API kvc_status kvc_profile_end(kvc_kernel_time* out, int32_t max_entries, int32_t* n_entries);
+
+/* ------------------------------------------------------------------ plan
+ * KV² page, "어떻게 동작하나": the first `sinks` tokens are kept as they are;
+ * the rest is split into chunks C_r = [sinks + r*m, min(sinks + (r+1)*m, N))
+ * and each chunk reconstructs n_q = max(floor(rho * |C_r|), 1) queries.
+ * Host-only.  `*n_chunks` receives M; if `chunk_off` is not NULL it must hold
+ * M + 1 host ints and receives the prefix sums of n_q (chunk_off[M] = Q).
+ * Invalid: N < 1, sinks < 0, sinks >= N, m < 1, rho outside (0, 1]. */
+KVC_API kvc_status kvc_chunk_plan(int32_t N, int32_t sinks, int32_t m, double rho, int32_t* n_chunks,
+                          int32_t* chunk_off);
+
+/* Kept tokens per (layer, KV head) for a budget fraction b in (0, 1]:
+ * floor(b * N), sinks included.  Host-only.  Invalid if the result is below
+ * `sinks` or above N. */
+KVC_API kvc_status kvc_budget_count(double b, int32_t N, int32_t sinks, int32_t* k);
+
+/* Bytes of workspace that every KV² entry point below (and kvc_compress)
+ * needs for this shape and chunk plan.  0 on invalid arguments. */
+KVC_API size_t kvc_workspace_size(kvc_shape shape, int32_t sinks, int32_t m, double rho);
+
+/* ------------------------------------------------------------------ stage 1
+ * KV² page, "어떻게 동작하나": KeyDiff proxy averaged over layers and KV heads.
+ * For each (layer, KV head): u = mean over all N positions of k_i / |k_i|,
+ * s_i = -(k_i . u) / (|k_i| |u|) (0 for a zero key or a zero u); then
+ * p_i = mean over the L*Hkv heads of s_i.
+ *   K      device bf16 [L][Hkv][N][d]
+ *   p      device f32 [N]                          (output)
+ *   s_opt  device f32 [L][Hkv][N] or NULL          (output)
+ *   ws     workspace of kvc_workspace_size() bytes */
+KVC_API kvc_status kvc_proxy_score(kvc_shape shape, const void* K, float* p, float* s_opt, void* ws, size_t ws_bytes,
+                           kvc_stream stream);
+
+/* KV² page, "어떻게 동작하나": inside each chunk the n_q positions with the
+ * highest p (the lower position wins a tie; NaN ranks lowest), written
+ * ascending, chunk after chunk.
+ *   p    device f32 [N]
+ *   sel  device int32 [Q], Q from kvc_chunk_plan   (output) */
+KVC_API kvc_status kvc_select_queries(int32_t N, int32_t sinks, int32_t m, double rho, const float* p, int32_t* sel,
+                              kvc_stream stream);
+
+/* ------------------------------------------------------------------ stage 2
+ * KV² page, "무엇과 다른가": the selected tokens are appended after the cache
+ * and run causally over the whole cache; the score of cache position i in
+ * C_r is the max, over the chunk's queries and over the query heads of the
+ * KV head, of the softmax attention paid to i.  For query j of chunk r and
+ * query head g the logits are q.k_i / sqrt(d) over the N cache keys followed
+ * by q.kapp_t / sqrt(d) for the chunk's appended keys t <= j.
+ *   K        device bf16 [L][Hkv][N][d]
+ *   Qpool    device bf16 [L][Hq][N][d]; query (g, j of chunk r) is row sel[off_r + j]
+ *   sel      device int32 [Q] from kvc_select_queries
+ *   Kapp_opt device bf16 [L][Hkv][Q][d] appended keys, or NULL to use K at sel
+ *   score    device f32 [L][Hkv][N] (output; positions < sinks are not written)
+ *   lse_opt  device f32 [L][Hq][Q] or NULL (output, natural log)
+ * Runs on the tensor cores (tcgen05, bf16 inputs, fp32 accumulation). */
+KVC_API kvc_status kvc_recon_score(kvc_shape shape, const void* K, const void* Qpool, const int32_t* sel, int32_t sinks,
+                           int32_t m, double rho, const void* Kapp_opt, float* score, float* lse_opt, void* ws,
+                           size_t ws_bytes, kvc_stream stream);
+
+/* KV² page, "무엇과 다른가" (iterative refinement): the stage-2 output has the
+ * proxy's token granularity, so p_i = mean over the L*Hkv heads of score_i
+ * replaces the proxy in the next pass.  p[i] = 0 for i < sinks.
+ *   score device f32 [L][Hkv][N]; p device f32 [N] (output) */
+KVC_API kvc_status kvc_refine_proxy(kvc_shape shape, const float* score, int32_t sinks, float* p, kvc_stream stream);
+
+/* KV² page, "무엇과 다른가": gather scores, pin the sink positions to the max
+ * score, remove the lowest-scored entries down to the budget.
+ *   score        device f32 [L][Hkv][N] (in/out: entries < sinks are
+ *                overwritten with the max over all entries >= sinks; they
+ *                are never read)
+ *   k_per_layer  HOST int32 [L], sinks <= k_l <= N
+ *   kept         device int32, ragged layer-major (output): the k_l kept
+ *                positions of each (l, h) in ascending order; the lower
+ *                position wins a tie, so the sinks are always kept. */
+KVC_API kvc_status kvc_evict_topk(kvc_shape shape, float* score, int32_t sinks, const int32_t* k_per_layer, int32_t* kept,
+                          void* ws, size_t ws_bytes, kvc_stream stream);
+
+/* KV² page, "전제와 한계": headwise compaction of the kept rows into a dense
+ * cache, Kc[l][h][t] = K[l][h][kept[l][h][t]] and likewise for V (bit copies).
+ *   K, V         device bf16 [L][Hkv][N][d]
+ *   kept         device int32 ragged (from kvc_evict_topk)
+ *   k_per_layer  HOST int32 [L]
+ *   Kc, Vc       device bf16 ragged (output); V/Vc may be NULL together */
+KVC_API kvc_status kvc_compact(kvc_shape shape, const void* K, const void* V, const int32_t* kept,
+                       const int32_t* k_per_layer, void* Kc, void* Vc, kvc_stream stream);
+
+/* Whole KV² compression: proxy, then `passes` rounds of query selection and
+ * reconstruction scoring (each round's mean score replacing the proxy),
+ * then eviction and compaction.  Outputs as in the entry points above;
+ * p_opt [N], sel_opt [Q] (last pass) and score_opt [L][Hkv][N] may be NULL
+ * (the workspace holds them then). */
+KVC_API kvc_status kvc_compress(kvc_shape shape, const void* K, const void* V, const void* Qpool, int32_t sinks, int32_t m,
+                        double rho, int32_t passes, const int32_t* k_per_layer, int32_t* kept, void* Kc, void* Vc,
+                        float* p_opt, int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes,
+                        kvc_stream stream);
+
+/* ------------------------------------------------------------------ EpiCache
+ * "[26'ICML] EpiCache", "+α: 레이어별 예산 배분": per-layer budgets from a
+ * sensitivity vector with sharpness alpha.  w_l = sens_l^alpha / sum_j
+ * sens_j^alpha; the L * mean_budget tokens are split by largest remainder
+ * (ties to the lower layer), then each budget is raised to at least `sinks`.
+ * Host-only.  sens: host f32 [L] (> 0); k_per_layer: host int32 [L]. */
+KVC_API kvc_status kvc_layer_budgets(const float* sens, int32_t L, double alpha, int64_t mean_budget, int32_t sinks,
+                             int32_t* k_per_layer);
+
+#define KVC_MAX_LAYERS 128
+
+/* State of one episode's block prefill.  Device buffers are caller-owned;
+ * the host fields are maintained by the library.  Every layer lives in one
+ * of two slabs (cur[l]); compaction moves the kept rows of a layer into the
+ * other slab, so a layer's rows are always at slab cur[l], rows [0, len[l]). */
+typedef struct {
+  int32_t L, Hkv, Hq, d;
+  int32_t capacity;               /* rows per (layer, KV head) in each slab: >= max budget + block */
+  int32_t sinks;
+  void* K[2];                     /* device bf16 [L][Hkv][capacity][d], two slabs */
+  void* V[2];                     /* device bf16 [L][Hkv][capacity][d], two slabs */
+  int32_t* pos[2];                /* device int32 [L][Hkv][capacity]: global position of each row */
+  int32_t cur[KVC_MAX_LAYERS];    /* host: slab holding layer l */
+  int32_t len[KVC_MAX_LAYERS];    /* host: rows held per layer (same for every KV head) */
+  int32_t budget[KVC_MAX_LAYERS]; /* host: M_l */
+  int64_t consumed;               /* host: history tokens consumed */
+} kvc_block_state;
+
+/* Initialises `st` for an empty cache (no device work).  Each slab must hold
+ * L*Hkv*capacity rows.  Invalid: L > KVC_MAX_LAYERS, d != 128, a budget
+ * below `sinks`, capacity below the largest budget. */
+KVC_API kvc_status kvc_block_state_init(kvc_block_state* st, int32_t L, int32_t Hkv, int32_t Hq, int32_t d, int32_t capacity,
+                                int32_t sinks, const int32_t* budgets, void* K0, void* V0, int32_t* pos0, void* K1,
+                                void* V1, int32_t* pos1);
+
+/* Workspace bytes for kvc_block_prefill_step with blocks of up to
+ * `max_block` tokens and P prompt queries. */
+KVC_API size_t kvc_block_workspace_size(const kvc_block_state* st, int32_t max_block, int32_t P);
+
+/* "[26'ICML] EpiCache", "방법: 3단계" step ② and Fig. 1(b,c): append one
+ * history block behind each layer's kept cache; every layer that then holds
+ * more than its budget M_l scores its non-sink rows against the episode's
+ * patched prompt (the KV² max rule with the prompt's P queries appended
+ * causally, prompt keys as the appended keys), pins the sinks, keeps the M_l
+ * best rows per KV head (lower global position wins a tie) in position
+ * order and compacts.  Peak cache size stays at M_l + block.
+ *   Kblk, Vblk  device bf16 [L][Hkv][blk_len][d]
+ *   Qprompt     device bf16 [L][Hq][P][d]
+ *   Kprompt     device bf16 [L][Hkv][P][d]
+ * Requires len[l] + blk_len <= capacity. */
+KVC_API kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk, const void* Vblk, int32_t blk_len,
+                                  const void* Qprompt, const void* Kprompt, int32_t P, void* ws, size_t ws_bytes,
+                                  kvc_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */

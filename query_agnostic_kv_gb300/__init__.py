@@ -1,0 +1,292 @@
+"""Python binding of libkvc.so -- attention-score KV-cache compression on
+GB300 (KV² selective reconstruction and EpiCache block prefill).
+
+Every function here has the name of the C entry point it calls and only
+marshals arguments: tensors become device pointers, the current torch CUDA
+stream becomes the library stream, and a non-OK status raises KVCError.  All
+compute runs in the library's CUDA kernels; nothing falls back to the CPU.
+If the library has not been built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "KVCError", "kvc_shape", "kvc_block_state", "lib", "shape_of",
+    "kvc_status_string", "kvc_device_check", "kvc_stream_status", "kvc_set_wait_limit_ns",
+    "kvc_debug_expire_wait", "kvc_chunk_plan", "kvc_budget_count", "kvc_workspace_size",
+    "kvc_proxy_score", "kvc_select_queries", "kvc_recon_score", "kvc_refine_proxy", "kvc_evict_topk",
+    "kvc_compact", "kvc_compress", "kvc_layer_budgets", "kvc_block_state_init",
+    "kvc_block_workspace_size", "kvc_block_prefill_step", "EXPORTED",
+]
+
+KVC_MAX_LAYERS = 128
+c_i32, c_i64, c_sz, c_vp, c_dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_double
+
+
+class kvc_shape(ctypes.Structure):
+    _fields_ = [("L", c_i32), ("Hkv", c_i32), ("Hq", c_i32), ("d", c_i32), ("N", c_i32)]
+
+
+class kvc_block_state(ctypes.Structure):
+    _fields_ = [("L", c_i32), ("Hkv", c_i32), ("Hq", c_i32), ("d", c_i32), ("capacity", c_i32), ("sinks", c_i32),
+                ("K", c_vp * 2), ("V", c_vp * 2), ("pos", c_vp * 2),
+                ("cur", c_i32 * KVC_MAX_LAYERS), ("len", c_i32 * KVC_MAX_LAYERS),
+                ("budget", c_i32 * KVC_MAX_LAYERS), ("consumed", c_i64)]
+
+
+class kvc_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", c_i32), ("total_ms", c_dbl)]
+
+
+class KVCError(RuntimeError):
+    def __init__(self, func: str, code: int):
+        self.code = code
+        super().__init__(f"{func}: {_status_text(code)}")
+
+
+# name -> (restype, argtypes)
+_SIGS = {
+    "kvc_status_string": (ctypes.c_char_p, [c_i32]),
+    "kvc_device_check": (c_i32, []),
+    "kvc_stream_status": (c_i32, [c_vp]),
+    "kvc_set_wait_limit_ns": (c_i32, [ctypes.c_uint64]),
+    "kvc_debug_expire_wait": (c_i32, [ctypes.c_uint64, c_vp]),
+    "kvc_chunk_plan": (c_i32, [c_i32, c_i32, c_i32, c_dbl, ctypes.POINTER(c_i32), ctypes.POINTER(c_i32)]),
+    "kvc_budget_count": (c_i32, [c_dbl, c_i32, c_i32, ctypes.POINTER(c_i32)]),
+    "kvc_workspace_size": (c_sz, [kvc_shape, c_i32, c_i32, c_dbl]),
+    "kvc_proxy_score": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_select_queries": (c_i32, [c_i32, c_i32, c_i32, c_dbl, c_vp, c_vp, c_vp]),
+    "kvc_recon_score": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_vp, c_vp, c_vp, c_vp, c_sz,
+                                c_vp]),
+    "kvc_refine_proxy": (c_i32, [kvc_shape, c_vp, c_i32, c_vp, c_vp]),
+    "kvc_evict_topk": (c_i32, [kvc_shape, c_vp, c_i32, ctypes.POINTER(c_i32), c_vp, c_vp, c_sz, c_vp]),
+    "kvc_compact": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, ctypes.POINTER(c_i32), c_vp, c_vp, c_vp]),
+    "kvc_compress": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_i32, ctypes.POINTER(c_i32), c_vp,
+                             c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_layer_budgets": (c_i32, [ctypes.POINTER(ctypes.c_float), c_i32, c_dbl, c_i64, c_i32,
+                                  ctypes.POINTER(c_i32)]),
+    "kvc_block_state_init": (c_i32, [ctypes.POINTER(kvc_block_state), c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                     ctypes.POINTER(c_i32), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "kvc_block_workspace_size": (c_sz, [ctypes.POINTER(kvc_block_state), c_i32, c_i32]),
+    "kvc_block_prefill_step": (c_i32, [ctypes.POINTER(kvc_block_state), c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_vp,
+                                       c_sz, c_vp]),
+    "kvc_profile_begin": (c_i32, []),
+    "kvc_profile_end": (c_i32, [ctypes.POINTER(kvc_kernel_time), c_i32, ctypes.POINTER(c_i32)]),
+}
+EXPORTED = tuple(_SIGS)
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libkvc.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                               "(the CUDA library is required; there is no fallback)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def _status_text(code: int) -> str:
+    try:
+        return lib().kvc_status_string(int(code)).decode()
+    except Exception:  # pragma: no cover
+        return f"status {code}"
+
+
+def _check(name: str, code: int) -> None:
+    if code != 0:
+        raise KVCError(name, code)
+
+
+def shape_of(L: int, Hkv: int, Hq: int, N: int, d: int = 128) -> kvc_shape:
+    return kvc_shape(L, Hkv, Hq, d, N)
+
+
+def _shape(s) -> kvc_shape:
+    if isinstance(s, kvc_shape):
+        return s
+    L, Hkv, Hq, d, N = s
+    return kvc_shape(L, Hkv, Hq, d, N)
+
+
+def _dev(t, dtype=None, name="tensor"):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return c_vp(t.data_ptr())
+
+
+def _ws(ws):
+    if ws is None:
+        return None, 0
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    return c_vp(ws.data_ptr()), ws.numel() * ws.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_vp(stream.cuda_stream)
+
+
+def _i32_array(vals: Sequence[int]):
+    return (c_i32 * len(vals))(*[int(v) for v in vals])
+
+
+# ---------------------------------------------------------------- status
+def kvc_status_string(code: int) -> str:
+    return lib().kvc_status_string(int(code)).decode()
+
+
+def kvc_device_check() -> None:
+    _check("kvc_device_check", lib().kvc_device_check())
+
+
+def kvc_stream_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device status code (0 = OK)."""
+    return int(lib().kvc_stream_status(_stream(stream)))
+
+
+def kvc_set_wait_limit_ns(limit_ns: int) -> None:
+    _check("kvc_set_wait_limit_ns", lib().kvc_set_wait_limit_ns(int(limit_ns)))
+
+
+def kvc_debug_expire_wait(limit_ns: int, stream=None) -> None:
+    _check("kvc_debug_expire_wait", lib().kvc_debug_expire_wait(int(limit_ns), _stream(stream)))
+
+
+def kvc_profile_begin() -> None:
+    _check("kvc_profile_begin", lib().kvc_profile_begin())
+
+
+def kvc_profile_end() -> dict:
+    """Synchronise and return {kernel name: (launches, total ms)}."""
+    arr = (kvc_kernel_time * 64)()
+    n = c_i32(0)
+    _check("kvc_profile_end", lib().kvc_profile_end(arr, 64, ctypes.byref(n)))
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(min(n.value, 64))}
+
+
+# ---------------------------------------------------------------- plans (host only)
+def kvc_chunk_plan(N: int, sinks: int, m: int, rho: float) -> list[int]:
+    """Prefix offsets of the per-chunk query counts (length M + 1)."""
+    n = c_i32(0)
+    _check("kvc_chunk_plan", lib().kvc_chunk_plan(N, sinks, m, float(rho), ctypes.byref(n), None))
+    off = (c_i32 * (n.value + 1))()
+    _check("kvc_chunk_plan", lib().kvc_chunk_plan(N, sinks, m, float(rho), ctypes.byref(n), off))
+    return list(off)
+
+
+def kvc_budget_count(b: float, N: int, sinks: int) -> int:
+    k = c_i32(0)
+    _check("kvc_budget_count", lib().kvc_budget_count(float(b), N, sinks, ctypes.byref(k)))
+    return k.value
+
+
+def kvc_workspace_size(shape, sinks: int, m: int, rho: float) -> int:
+    return int(lib().kvc_workspace_size(_shape(shape), sinks, m, float(rho)))
+
+
+def kvc_layer_budgets(sens: Sequence[float], alpha: float, mean_budget: int, sinks: int) -> list[int]:
+    L = len(sens)
+    s = (ctypes.c_float * L)(*[float(x) for x in sens])
+    out = (c_i32 * L)()
+    _check("kvc_layer_budgets", lib().kvc_layer_budgets(s, L, float(alpha), int(mean_budget), sinks, out))
+    return list(out)
+
+
+# ---------------------------------------------------------------- KV² stages
+def kvc_proxy_score(shape, K, p, s=None, ws=None, stream=None) -> None:
+    w, wb = _ws(ws)
+    _check("kvc_proxy_score", lib().kvc_proxy_score(_shape(shape), _dev(K, torch.bfloat16, "K"),
+                                                    _dev(p, torch.float32, "p"), _dev(s, torch.float32, "s"),
+                                                    w, wb, _stream(stream)))
+
+
+def kvc_select_queries(N, sinks, m, rho, p, sel, stream=None) -> None:
+    _check("kvc_select_queries", lib().kvc_select_queries(N, sinks, m, float(rho), _dev(p, torch.float32, "p"),
+                                                          _dev(sel, torch.int32, "sel"), _stream(stream)))
+
+
+def kvc_recon_score(shape, K, Qpool, sel, sinks, m, rho, score, Kapp=None, lse=None, ws=None, stream=None) -> None:
+    w, wb = _ws(ws)
+    _check("kvc_recon_score", lib().kvc_recon_score(
+        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev(Qpool, torch.bfloat16, "Qpool"),
+        _dev(sel, torch.int32, "sel"), sinks, m, float(rho), _dev(Kapp, torch.bfloat16, "Kapp"),
+        _dev(score, torch.float32, "score"), _dev(lse, torch.float32, "lse"), w, wb, _stream(stream)))
+
+
+def kvc_refine_proxy(shape, score, sinks, p, stream=None) -> None:
+    _check("kvc_refine_proxy", lib().kvc_refine_proxy(_shape(shape), _dev(score, torch.float32, "score"), sinks,
+                                                      _dev(p, torch.float32, "p"), _stream(stream)))
+
+
+def kvc_evict_topk(shape, score, sinks, k_per_layer, kept, ws=None, stream=None) -> None:
+    w, wb = _ws(ws)
+    _check("kvc_evict_topk", lib().kvc_evict_topk(_shape(shape), _dev(score, torch.float32, "score"), sinks,
+                                                  _i32_array(k_per_layer), _dev(kept, torch.int32, "kept"), w, wb,
+                                                  _stream(stream)))
+
+
+def kvc_compact(shape, K, V, kept, k_per_layer, Kc, Vc, stream=None) -> None:
+    _check("kvc_compact", lib().kvc_compact(_shape(shape), _dev(K, torch.bfloat16, "K"),
+                                            _dev(V, torch.bfloat16, "V"), _dev(kept, torch.int32, "kept"),
+                                            _i32_array(k_per_layer), _dev(Kc, torch.bfloat16, "Kc"),
+                                            _dev(Vc, torch.bfloat16, "Vc"), _stream(stream)))
+
+
+def kvc_compress(shape, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, Kc, Vc, p=None, sel=None,
+                 score=None, ws=None, stream=None) -> None:
+    w, wb = _ws(ws)
+    _check("kvc_compress", lib().kvc_compress(
+        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev(V, torch.bfloat16, "V"),
+        _dev(Qpool, torch.bfloat16, "Qpool"), sinks, m, float(rho), passes, _i32_array(k_per_layer),
+        _dev(kept, torch.int32, "kept"), _dev(Kc, torch.bfloat16, "Kc"), _dev(Vc, torch.bfloat16, "Vc"),
+        _dev(p, torch.float32, "p"), _dev(sel, torch.int32, "sel"), _dev(score, torch.float32, "score"), w, wb,
+        _stream(stream)))
+
+
+# ---------------------------------------------------------------- EpiCache block prefill
+def kvc_block_state_init(L, Hkv, Hq, capacity, sinks, budgets, K0, V0, pos0, K1, V1, pos1,
+                         d: int = 128) -> kvc_block_state:
+    st = kvc_block_state()
+    _check("kvc_block_state_init", lib().kvc_block_state_init(
+        ctypes.byref(st), L, Hkv, Hq, d, capacity, sinks, _i32_array(budgets),
+        _dev(K0, torch.bfloat16, "K0"), _dev(V0, torch.bfloat16, "V0"), _dev(pos0, torch.int32, "pos0"),
+        _dev(K1, torch.bfloat16, "K1"), _dev(V1, torch.bfloat16, "V1"), _dev(pos1, torch.int32, "pos1")))
+    return st
+
+
+def kvc_block_workspace_size(state: kvc_block_state, max_block: int, P: int) -> int:
+    return int(lib().kvc_block_workspace_size(ctypes.byref(state), max_block, P))
+
+
+def kvc_block_prefill_step(state: kvc_block_state, Kblk, Vblk, blk_len, Qprompt, Kprompt, P, ws=None,
+                           stream=None) -> None:
+    w, wb = _ws(ws)
+    _check("kvc_block_prefill_step", lib().kvc_block_prefill_step(
+        ctypes.byref(state), _dev(Kblk, torch.bfloat16, "Kblk"), _dev(Vblk, torch.bfloat16, "Vblk"), blk_len,
+        _dev(Qprompt, torch.bfloat16, "Qprompt"), _dev(Kprompt, torch.bfloat16, "Kprompt"), P, w, wb,
+        _stream(stream)))

@@ -1,0 +1,164 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxLayers = KVC_MAX_LAYERS;
+
+// Per-device status word (device address) and the process-wide wait limit.
+int* status_word();
+uint64_t wait_limit_ns();
+int num_sms();
+
+// Per-kernel event timing (active between kvc_profile_begin/end): brackets
+// the launches made during the scope's lifetime with an event pair.
+struct ProfScope {
+  int slot = -1;
+  cudaStream_t stream = nullptr;
+  ProfScope(const char* name, cudaStream_t st);
+  ~ProfScope();
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+};
+
+// Chunk plan on the host (same rule as kvc_chunk_plan).
+struct ChunkPlan {
+  int32_t n_chunks = 0;
+  int32_t nq_full = 0;   // n_q of every chunk but the last
+  int32_t nq_last = 0;   // n_q of the last chunk
+  int32_t Q = 0;         // total reconstruction queries
+  int32_t m = 0;         // chunk size
+  int32_t last_len = 0;  // |C_last|
+};
+bool make_plan(int32_t N, int32_t sinks, int32_t m, double rho, ChunkPlan* plan);
+
+// Workspace carving: 256-B aligned slices out of one caller buffer.
+struct Carver {
+  char* base;
+  size_t cap;
+  size_t used = 0;
+  bool ok = true;
+  Carver(void* b, size_t c) : base(static_cast<char*>(b)), cap(c) {}
+  template <class T>
+  T* take(size_t count) {
+    size_t off = (used + 255) & ~size_t(255);
+    size_t bytes = count * sizeof(T);
+    if (off + bytes > cap || (base == nullptr && bytes > 0)) {
+      ok = false;
+      used = off + bytes;
+      return nullptr;
+    }
+    used = off + bytes;
+    return reinterpret_cast<T*>(base + off);
+  }
+};
+
+// 2-D bf16 tensor map over `rows` rows of 128 elements, box = 64 x box_rows,
+// 128-byte swizzle (the K-major tcgen05 operand layout).
+bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
+
+// ------------------------------------------------------------------ launchers
+// Each returns cudaSuccess or the launch error.
+
+// KeyDiff proxy: s[lh][i] for LH = L*Hkv heads of N rows, then p = mean.
+cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, cudaStream_t st);
+
+// p[i] = mean over LH rows of x[lh][i] (stride ld); p[i] = 0 for i < zero_below.
+cudaError_t launch_mean_heads(const float* x, int LH, int N, int64_t ld, int zero_below, float* p,
+                              cudaStream_t st);
+
+// Per-chunk selection of reconstruction queries.
+cudaError_t launch_select(const float* p, int N, int sinks, const ChunkPlan& plan, double rho, int32_t* sel,
+                          cudaStream_t st);
+
+// Row-wise eviction: for every (l, h) keep sinks + top (k_l - sinks) of
+// score[l][h][sinks:n_l); kept rows written at out_off[l] + h*k_l.
+struct EvictParams {
+  int L, Hkv, sinks;
+  int64_t ld;                     // row stride of score
+  int32_t n[kMaxLayers];          // scored length per layer
+  int32_t k[kMaxLayers];          // kept per (l, h)
+  int64_t out_off[kMaxLayers];    // output offset of layer l
+  int32_t active[kMaxLayers];     // 0: layer skipped
+};
+cudaError_t launch_evict(float* score, const EvictParams& ep, int32_t* kept, uint32_t* gmax_word, bool pin,
+                         cudaStream_t st);
+
+// Compaction: dst row (l, h, t) = src row (l, h, idx[l][h][t]).
+struct CompactParams {
+  int L, Hkv;
+  int64_t src_ld;                 // rows per (l, h) in the source
+  int64_t dst_ld;                 // rows per (l, h) in the destination; <0: ragged (use dst_off)
+  int32_t n_src[kMaxLayers];      // valid source rows per layer (bounds check)
+  int32_t k[kMaxLayers];
+  int64_t idx_off[kMaxLayers];    // offset of layer l in the index array
+  int64_t dst_off[kMaxLayers];    // ragged destination offset (rows) of layer l
+  int32_t active[kMaxLayers];
+};
+cudaError_t launch_compact(const void* K, const void* V, const int32_t* idx, const int32_t* pos_src,
+                           int32_t* pos_dst, void* Kc, void* Vc, const CompactParams& cp, cudaStream_t st);
+
+// Block append: state rows [len_l, len_l + B) of each (l, h) <- block rows.
+struct AppendParams {
+  int L, Hkv, B;
+  int64_t ld;                     // rows per (l, h) in the state slab
+  int32_t len[kMaxLayers];
+  int32_t cur[kMaxLayers];        // which of the two slabs holds layer l
+  int64_t pos0;                   // global position of the block's first token
+};
+cudaError_t launch_append(const void* Kblk, const void* Vblk, void* K0, void* V0, int32_t* pos0, void* K1, void* V1,
+                          int32_t* pos1, const AppendParams& ap, cudaStream_t st);
+
+// Reconstruction scoring on the tensor cores.
+struct ReconLayer {
+  int32_t layer;     // model layer index
+  int32_t n;         // cache rows of this layer
+  int32_t m;         // chunk size of this layer
+  int32_t n_chunks;  // chunks of this layer
+  int32_t last_len;  // size of the last chunk
+  int32_t slab;      // which K slab (0/1) holds the layer (block prefill); 0 otherwise
+};
+struct ReconProblem {
+  int L, Hkv, Hq, G, sinks;
+  int n_active;
+  ReconLayer lay[kMaxLayers];
+  // cache keys: base[slab] + ((layer*Hkv + h) * ldK + row) * d
+  const void* K[2];
+  int64_t ldK;
+  // query source rows: Qsrc + ((layer*Hq + g) * ldQ + src) * d, src = sel ? sel[t] : t
+  const void* Qsrc;
+  int64_t ldQ;
+  const int32_t* sel;
+  // appended keys: Kapp + ((layer*Hkv + h) * ldApp + t) * d, or gathered from K at sel if Kapp is null
+  const void* Kapp;
+  int64_t ldApp;
+  // chunk query counts (same for every layer)
+  int32_t nq_full, nq_last, Q;
+  // outputs
+  float* score;       // score + (layer*Hkv + h) * ldS + position
+  int64_t ldS;
+  float* lse_out;     // optional [L][Hq][Q], natural log
+};
+struct ReconWorkspace {
+  void* Qg;       // bf16 [L*Hkv][Rpad][d]
+  void* Kg;       // bf16 [L*Hkv][Q][d] (gathered appended keys), when Kapp is null
+  float* lse2;    // f32 [L*Hkv][Rpad] (log2 units)
+  int32_t Rpad;   // rows per (l, h) in Qg, multiple of 128
+};
+// Rows per (layer, KV head) of the query row space (chunks padded to 128 rows).
+int32_t recon_rows(int G, int n_chunks, int nq_full, int nq_last);
+size_t recon_ws_bytes(int L, int Hkv, int G, int n_chunks, int nq_full, int nq_last, int Q, bool need_kg);
+cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaStream_t st);
+
+// Device-side wait that expires on purpose (status-path test).
+cudaError_t launch_expire_wait(uint64_t limit_ns, cudaStream_t st);
+
+}  // namespace kvc

@@ -1,0 +1,97 @@
+"""The C-ABI library on the host: it builds, loads, exports every symbol
+declared in include/kvc.h, and its host-only functions (chunk plan, budget
+count, layer budgets, argument validation) agree with the oracle.  No
+device compute is called here."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import __graft_entry__ as ge
+import kv_synth as ks
+from oracle import kv2
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qk():
+    ge.build()
+    import query_agnostic_kv_gb300 as q
+    return q
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    return sorted(set(re.findall(r"^KVC_API\s+[\w\s\*]*?\b(kvc_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_all_entry_points():
+    names = declared_symbols()
+    for n in ("kvc_proxy_score", "kvc_select_queries", "kvc_recon_score", "kvc_evict_topk", "kvc_compact",
+              "kvc_block_prefill_step", "kvc_layer_budgets", "kvc_compress"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(qk):
+    import subprocess
+    lib = qk.lib()
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", qk._build.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (kvc_\w+)", out))
+    assert set(declared_symbols()) <= exported
+    assert set(qk.EXPORTED) == set(declared_symbols())
+
+
+@pytest.mark.parametrize("N,S,m,rho", [(4096, 4, 1024, 0.1), (16384, 4, 4096, 0.1), (32768, 4, 4096, 0.25),
+                                       (131072, 4, 4096, 0.5), (20, 4, 64, 0.01), (12, 2, 4, 1.0),
+                                       (1000, 0, 7, 0.333), (90000, 4, 89996, 0.5)])
+def test_chunk_plan_matches_oracle(qk, N, S, m, rho):
+    off = qk.kvc_chunk_plan(N, S, m, rho)
+    ch = kv2.chunk_plan(N, S, m, rho)
+    assert off == [c.off for c in ch] + [sum(c.nq for c in ch)]
+
+
+def test_budget_count_matches_oracle(qk):
+    for b, N in [(0.05, 4096), (0.02, 16384), (0.05, 32768), (0.1, 131072), (0.3, 1000), (1.0, 77)]:
+        assert qk.kvc_budget_count(b, N, 4) == kv2.budget_count(b, N)
+
+
+@pytest.mark.parametrize("alpha", [0.0, 1.0, 2.0, 3.0, 4.0, 8.0])
+def test_layer_budgets_match_oracle(qk, alpha):
+    sens = ks.gen_sensitivity(ks.EPI_3B)
+    got = qk.kvc_layer_budgets(sens.tolist(), alpha, 8192, 4)
+    ref = kv2.layer_budgets(sens.astype(np.float64), alpha, 8192, 4)
+    assert got == ref.tolist()
+
+
+def test_layer_budgets_golden(qk):
+    import json
+    for c in json.load(open(os.path.join(ROOT, "tests", "golden", "layer_budgets.json")))["cases"]:
+        assert qk.kvc_layer_budgets(c["sens"], c["alpha"], c["M"], c["S"]) == c["budgets"]
+
+
+def test_invalid_arguments_rejected_on_host(qk):
+    with pytest.raises(qk.KVCError) as e:
+        qk.kvc_chunk_plan(100, 4, 16, 0.0)
+    assert e.value.code == 1
+    with pytest.raises(qk.KVCError):
+        qk.kvc_chunk_plan(100, 100, 16, 0.5)        # sinks >= N
+    with pytest.raises(qk.KVCError):
+        qk.kvc_chunk_plan(100, 4, 0, 0.5)           # m < 1
+    with pytest.raises(qk.KVCError):
+        qk.kvc_chunk_plan(100, 4, 16, 1.5)          # rho > 1
+    with pytest.raises(qk.KVCError):
+        qk.kvc_budget_count(0.01, 100, 4)           # below sinks
+    with pytest.raises(qk.KVCError):
+        qk.kvc_layer_budgets([1.0, -1.0], 2.0, 10, 0)
+    assert qk.kvc_workspace_size((1, 1, 4, 64, 128), 4, 16, 0.5) == 0     # d != 128
+    assert qk.kvc_workspace_size((1, 2, 3, 128, 128), 4, 16, 0.5) == 0    # Hq % Hkv
+    assert qk.kvc_workspace_size((1, 1, 4, 128, 4096), 4, 1024, 0.1) > 0
+
+
+def test_status_strings(qk):
+    for code in range(7):
+        assert qk.kvc_status_string(code).startswith("KVC_")
