@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--config", default=ks.LLAMA_16K.name, choices=list(ks.KV2_CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="use only this many layers (profiling cases)")
     return ap.parse_args()
 
 
@@ -412,6 +413,8 @@ def run_ours(args, cfg, rank, world, local_rank):
 def main():
     args = parse()
     cfg = ks.KV2_CONFIGS[args.config]
+    if args.layers:
+        cfg = ks.scaled(cfg, name=f"{cfg.name}-{args.layers}layers", L=args.layers)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
