@@ -136,6 +136,23 @@ KVC_API size_t kvc_workspace_size(kvc_shape shape, int32_t sinks, int32_t m, dou
 KVC_API kvc_status kvc_proxy_score(kvc_shape shape, const void* K, float* p, float* s_opt, void* ws, size_t ws_bytes,
                            kvc_stream stream);
 
+/* The pages have no counterpart to this entry point.  Same result as
+ * kvc_proxy_score (p only) for callers that cannot allocate device memory
+ * when they need the proxy -- runtimes that give all free HBM to their own
+ * pool allocator, or hot paths that must not call cudaMalloc because it can
+ * synchronise the device.  The per-head scratch lives in a 16 MiB array
+ * inside the library, reserved on each GPU the first time the library's
+ * module is loaded there and held until the process exits; this call
+ * allocates nothing.  Limit: L*Hkv*N <= 4194304 (e.g. 32 layers x 8 KV
+ * heads x 16384 tokens); larger shapes return KVC_ERR_WORKSPACE before any
+ * launch.  The first call on a device looks up the array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  All calls on a device share the array: calls that
+ * may overlap on the GPU race and must be ordered by the caller.  No part of
+ * the array needs clearing between calls.
+ *   K  device bf16 [L][Hkv][N][d];  p  device f32 [N] (output) */
+KVC_API kvc_status kvc_proxy_score_noalloc(kvc_shape shape, const void* K, float* p, kvc_stream stream);
+
 /* KV² page, "어떻게 동작하나": inside each chunk the n_q positions with the
  * highest p (the lower position wins a tie; NaN ranks lowest), written
  * ascending, chunk after chunk.

@@ -77,6 +77,7 @@ _SIGS = {
     "kvc_block_workspace_size": (c_sz, [ctypes.POINTER(kvc_block_state), c_i32, c_i32]),
     "kvc_block_prefill_step": (c_i32, [ctypes.POINTER(kvc_block_state), c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_vp,
                                        c_sz, c_vp]),
+    "kvc_proxy_score_noalloc": (c_i32, [kvc_shape, c_vp, c_vp, c_vp]),
     "kvc_profile_begin": (c_i32, []),
     "kvc_profile_end": (c_i32, [ctypes.POINTER(kvc_kernel_time), c_i32, ctypes.POINTER(c_i32)]),
 }
@@ -223,6 +224,15 @@ def kvc_proxy_score(shape, K, p, s=None, ws=None, stream=None) -> None:
     _check("kvc_proxy_score", lib().kvc_proxy_score(_shape(shape), _dev(K, torch.bfloat16, "K"),
                                                     _dev(p, torch.float32, "p"), _dev(s, torch.float32, "s"),
                                                     w, wb, _stream(stream)))
+
+
+def kvc_proxy_score_noalloc(shape, K, p, stream=None) -> None:
+    """kvc_proxy_score without a workspace: for callers that cannot allocate
+    device memory at this point (their runtime owns all free HBM, or the call
+    sits on a path where cudaMalloc is not allowed).  Scratch comes from a
+    16 MiB array inside the library; L*Hkv*N must not exceed 4194304."""
+    _check("kvc_proxy_score_noalloc", lib().kvc_proxy_score_noalloc(
+        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev(p, torch.float32, "p"), _stream(stream)))
 
 
 def kvc_select_queries(N, sinks, m, rho, p, sel, stream=None) -> None:
