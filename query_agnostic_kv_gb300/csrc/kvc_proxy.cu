@@ -24,10 +24,11 @@ namespace kvc {
 namespace {
 
 constexpr int CLUSTER = 8;
-constexpr int THREADS = 1024;
-constexpr int HALVES = THREADS / 16;      // half-warps per CTA: rows in flight per step
-constexpr int UNROLL = 4;                 // rows per half-warp per step
-constexpr int CACHE_ROWS = 768;           // rows of the slice kept in shared memory (192 KB)
+constexpr int THREADS = 512;
+constexpr int CTAS_PER_SM = 2;            // two clusters' CTAs share an SM: one loads while the other waits
+constexpr int HALVES = THREADS / 16;      // half-warps per CTA
+constexpr int UNROLL = 8;                 // rows per half-warp in flight per step (64 KB per CTA)
+constexpr int CACHE_ROWS = 256;           // rows of the slice kept in shared memory for pass B (64 KB)
 constexpr int SMEM_BYTES = CACHE_ROWS * 256 + HALVES * 128 * 4;
 
 __device__ __forceinline__ void unpack8(const uint4& q, float (&f)[8]) {
@@ -48,7 +49,7 @@ __device__ __forceinline__ float half_warp_sum(float v) {
   return v;
 }
 
-__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_PER_SM)
     keydiff_kernel(const __nv_bfloat16* __restrict__ K, int N, float* __restrict__ s_out) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint4* cache = reinterpret_cast<uint4*>(smem);                            // [CACHE_ROWS][16]

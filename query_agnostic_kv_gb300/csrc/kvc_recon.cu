@@ -5,20 +5,25 @@
 // the softmax attention it receives.
 //
 // Two tensor-core passes per (layer, KV head), both on one warp-specialised
-// skeleton (warp 0: TMA producer, warp 1: tcgen05.mma issuer and TMEM owner,
-// warps 2-9: two consumer warpgroups):
+// persistent skeleton (warp 0: TMA producer, warp 1: tcgen05.mma issuer and
+// TMEM owner, then 4 warps per A tile as consumers):
 //
-//   pass 1 (row LSE)   A = 2 tiles of 128 reconstruction-query rows, B =
-//                      streamed 128-key tiles of the cache, then the chunk's
-//                      appended keys under the causal mask.  Each consumer
-//                      thread owns one query row (one TMEM lane) and keeps an
-//                      online max / sum of 2^x, ending with
-//                      lse2 = max + log2(sum) (log2 units).
+//   pass 1 (row LSE)    A = 4 tiles of 128 reconstruction-query rows, B =
+//                       streamed 128-key tiles of the cache, then the chunk's
+//                       appended keys under the causal mask.  Each consumer
+//                       thread owns one query row (one TMEM lane) and keeps an
+//                       online max / sum of 2^x: lse2 = max + log2(sum).
+//                       On GB300 the MUFU exp2 rate (32/clk/SM) equals the
+//                       MMA logit rate at d = 128, so 16 consumer warps (4
+//                       per SM sub-partition) keep the exponentials flowing
+//                       while single-buffered accumulators are handed back to
+//                       the MMA warp as soon as they are read.
 //   pass 2 (column max) A = 2 tiles of 128 cache keys of one chunk, B = the
-//                      chunk's query rows.  Each consumer thread owns one key
-//                      (TMEM lane) and folds max_j (x_ij - lse2_j) over every
-//                      query column; exp2 is monotone, so one exp2 per key
-//                      gives the max attention.  One store per position.
+//                       chunk's query rows, double-buffered accumulators.
+//                       Each consumer thread owns one key (TMEM lane) and
+//                       folds max_j (x_ij - lse2_j) over every query column;
+//                       exp2 is monotone, so one exp2 per key gives the max
+//                       attention.  One store per position.
 //
 // Query rows are laid out per (layer, KV head) in a "row space": chunk r
 // occupies rows [r*CR, r*CR + G*nq_r) ordered (query head g, query j), with
@@ -35,14 +40,50 @@
 namespace kvc {
 namespace {
 
-constexpr int TILE_ROWS = 128;                 // rows of every A and B tile
-constexpr int TILE_BYTES = TILE_ROWS * 256;    // 128 rows x 128 bf16
-constexpr int HALF_BYTES = TILE_BYTES / 2;     // one 64-column swizzled half
-constexpr int KSTAGES = 3;                     // B-tile ring depth
-constexpr int NUM_THREADS = 320;               // 10 warps
-constexpr uint32_t TMEM_COLS = 512;            // 2 buffers x 2 accumulators x 128 columns
-constexpr int SMEM_TILES = 4 + KSTAGES;        // A[2][2] + B ring
-constexpr int SMEM_BYTES = 1024 + SMEM_TILES * TILE_BYTES + 256;
+constexpr int TILE_ROWS = 128;                  // rows of an A tile (TMEM lanes)
+constexpr int TILE_BYTES = TILE_ROWS * 256;     // 128 rows x 128 bf16
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int LSE_STAGE_BYTES = 128 * 4;        // pass 2: lse2 of the B tile's 128 query rows
+constexpr int MAX_KST = 3;
+
+// Per-pass shape of the pipeline.  B tiles of 256 rows (MMA N = 256) halve
+// the A-operand re-reads from shared memory per FLOP; with N = 128 the
+// shared-memory operand traffic, not the tensor core, caps the MMA rate.
+template <int PASS>
+struct Cfg;
+template <>
+struct Cfg<1> {
+  static constexpr int NA = 2;      // A tiles (128 query rows each) per unit
+  static constexpr int ABUF = 1;    // A buffers
+  static constexpr int DBUF = 1;    // accumulator buffers per A tile
+  static constexpr int BN = 256;    // rows (keys) of a B tile = MMA N
+  static constexpr int CSPLIT = 2;  // consumer warps sharing one TMEM lane quarter (column split)
+  static constexpr int KST = 2;     // B-tile ring depth
+};
+template <>
+struct Cfg<2> {
+  static constexpr int NA = 2;
+  static constexpr int ABUF = 2;
+  static constexpr int DBUF = 2;
+  static constexpr int BN = 128;
+  static constexpr int CSPLIT = 1;
+  static constexpr int KST = 3;
+};
+template <int PASS>
+constexpr int kThreads = 64 + 128 * Cfg<PASS>::NA * Cfg<PASS>::CSPLIT;
+template <int PASS>
+constexpr int kABytes = Cfg<PASS>::ABUF * Cfg<PASS>::NA * TILE_BYTES;
+template <int PASS>
+constexpr int kBStage = Cfg<PASS>::BN * 256;
+template <int PASS>
+constexpr int kCombBytes = Cfg<PASS>::CSPLIT > 1 ? Cfg<PASS>::NA * TILE_ROWS * 8 : 0;
+template <int PASS>
+constexpr int kSmemBytes = 1024 + kABytes<PASS> + Cfg<PASS>::KST * (kBStage<PASS> + LSE_STAGE_BYTES) +
+                           kCombBytes<PASS> + 256;
+static_assert(Cfg<1>::NA * Cfg<1>::DBUF * Cfg<1>::BN <= TMEM_COLS, "TMEM pass 1");
+static_assert(Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_COLS, "TMEM pass 2");
+static_assert(kSmemBytes<1> <= 232448 && kSmemBytes<2> <= 232448, "shared memory budget of one CTA");
+static_assert(Cfg<1>::KST <= MAX_KST && Cfg<2>::KST <= MAX_KST, "ring depth");
 
 struct KParams {
   int Hkv, Hq, G, sinks;
@@ -58,7 +99,7 @@ struct KParams {
   int32_t nq_full, nq_last, Q;
   int32_t CR, Rpad;                   // row-space chunk stride and rows per (l, h)
   int32_t ldApp;                      // appended-key rows per (l, h)
-  int32_t pairs1;                     // pass-1 units per (l, h): ceil(Rpad / 256)
+  int32_t units1;                     // pass-1 units per (l, h)
   int n_units;
   float scale_log2;                   // log2(e) / sqrt(d)
   float* lse2;
@@ -80,6 +121,41 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// Software exp2 (Cody-Waite range reduction + minimax polynomial, the split
+// of exponentials between MUFU and the FMA pipe used by FlashAttention-4):
+// x = n + f with n = round(x) (via the 1.5 * 2^23 rounding constant),
+// f in [-0.5, 0.5], 2^f ~= C0 + f (C1 + f (C2 + f C3)) with max relative
+// error 7.5e-5 (coefficients from csrc/fit_exp2_poly.py), 2^n added to the
+// exponent bits; x is clamped at -125 so that 2^n * p stays a normal number
+// (terms that small are below fp32 resolution of the row sum).  On GB300 the
+// MUFU exp2 rate already matches the MMA, and moving 3/8 of the
+// exponentials here measured 13% slower, so EMU_PAIRS is 0.
+constexpr float EXP2_C0 = 0.9999280571937561f;
+constexpr float EXP2_C1 = 0.6932609677314758f;
+constexpr float EXP2_C2 = 0.2426111251115799f;
+constexpr float EXP2_C3 = 0.0551716685295105f;
+constexpr float ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23
+constexpr int EMU_PAIRS = 0;                // column pairs (of 32 per 64-column half) on the FMA pipe
+
+__device__ __forceinline__ uint64_t exp2_poly2(float x0, float x1) {
+  x0 = fmaxf(x0, -125.0f);
+  x1 = fmaxf(x1, -125.0f);
+  const uint64_t x = pack2(x0, x1);
+  const uint64_t t = add2(x, pack2(ROUND_MAGIC, ROUND_MAGIC));    // magic + n, exact
+  const uint64_t n = add2(t, pack2(-ROUND_MAGIC, -ROUND_MAGIC));  // n as float
+  const uint64_t f = fma2(n, pack2(-1.0f, -1.0f), x);              // x - n
+  uint64_t p = fma2(pack2(EXP2_C3, EXP2_C3), f, pack2(EXP2_C2, EXP2_C2));
+  p = fma2(p, f, pack2(EXP2_C1, EXP2_C1));
+  p = fma2(p, f, pack2(EXP2_C0, EXP2_C0));
+  float p0, p1, t0, t1;
+  unpack2(p, p0, p1);
+  unpack2(t, t0, t1);
+  // the low mantissa bits of t hold n; shifted into the exponent field
+  const float r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
+  const float r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
+  return pack2(r0, r1);
+}
+
 __device__ __forceinline__ int nq_of(const KParams& P, int ai, int r) {
   return (r == P.n_chunks[ai] - 1) ? P.nq_last : P.nq_full;
 }
@@ -87,7 +163,7 @@ __device__ __forceinline__ int nq_of(const KParams& P, int ai, int r) {
 // ----------------------------------------------------------------- units
 struct Unit {
   int ai, layer, h, lh, slab, n;
-  int has1;        // second A tile present
+  int ntile;       // A tiles present (1..NA)
   // pass 1
   int R0, R1;      // row-space range [R0, R1] of the unit (inclusive)
   int ra, rb;      // chunk range touching the unit
@@ -97,7 +173,6 @@ struct Unit {
   int nT;          // B tiles of the unit
 };
 
-template <int PASS>
 __device__ __forceinline__ bool chunk_has_rows(const KParams& P, int ai, int r, int R0, int R1) {
   const int a = r * P.CR, b = r * P.CR + P.G * nq_of(P, ai, r) - 1;
   return a <= R1 && b >= R0;
@@ -105,27 +180,29 @@ __device__ __forceinline__ bool chunk_has_rows(const KParams& P, int ai, int r, 
 
 template <int PASS>
 __device__ Unit decode_unit(const KParams& P, int u) {
+  constexpr int NA = Cfg<PASS>::NA;
   Unit U;
   if (PASS == 1) {
-    const int per_layer = P.Hkv * P.pairs1;
+    const int per_layer = P.Hkv * P.units1;
     U.ai = u / per_layer;
     const int rem = u - U.ai * per_layer;
-    U.h = rem / P.pairs1;
-    const int pp = rem - U.h * P.pairs1;
+    U.h = rem / P.units1;
+    const int q = rem - U.h * P.units1;
     U.layer = P.layer[U.ai];
     U.lh = U.layer * P.Hkv + U.h;
     U.slab = P.slab[U.ai];
     U.n = P.n[U.ai];
-    U.R0 = pp * 2 * TILE_ROWS;
-    U.R1 = min(U.R0 + 2 * TILE_ROWS, P.Rpad) - 1;
-    U.has1 = (U.R0 + TILE_ROWS) < P.Rpad;
+    U.R0 = q * NA * TILE_ROWS;
+    U.R1 = min(U.R0 + NA * TILE_ROWS, P.Rpad) - 1;
+    U.ntile = (U.R1 - U.R0) / TILE_ROWS + 1;
     const int nc = P.n_chunks[U.ai];
     U.ra = min(U.R0 / P.CR, nc - 1);
     U.rb = min(U.R1 / P.CR, nc - 1);
-    U.nK = (U.n + TILE_ROWS - 1) / TILE_ROWS;
+    constexpr int BN = Cfg<1>::BN;
+    U.nK = (U.n + BN - 1) / BN;
     int nt = U.nK;
     for (int r = U.ra; r <= U.rb; ++r)
-      if (chunk_has_rows<1>(P, U.ai, r, U.R0, U.R1)) nt += (nq_of(P, U.ai, r) + TILE_ROWS - 1) / TILE_ROWS;
+      if (chunk_has_rows(P, U.ai, r, U.R0, U.R1)) nt += (nq_of(P, U.ai, r) + BN - 1) / BN;
     U.nT = nt;
     U.r = U.lo = U.hi = U.key0 = 0;
   } else {
@@ -136,27 +213,28 @@ __device__ Unit decode_unit(const KParams& P, int u) {
     U.slab = P.slab[ai];
     U.n = P.n[ai];
     const int m = P.m[ai], nc = P.n_chunks[ai];
-    const int pf = (m + 2 * TILE_ROWS - 1) / (2 * TILE_ROWS);
-    const int pl = (P.last_len[ai] + 2 * TILE_ROWS - 1) / (2 * TILE_ROWS);
+    constexpr int span = NA * TILE_ROWS;
+    const int pf = (m + span - 1) / span;
+    const int pl = (P.last_len[ai] + span - 1) / span;
     const int per_head = (nc - 1) * pf + pl;
     const int rem = u - P.unit_off[ai];
     U.h = rem / per_head;
     const int q = rem - U.h * per_head;
     U.lh = U.layer * P.Hkv + U.h;
-    int r, kp;
+    int r, kq;
     if (q < (nc - 1) * pf) {
       r = q / pf;
-      kp = q - r * pf;
+      kq = q - r * pf;
     } else {
       r = nc - 1;
-      kp = q - (nc - 1) * pf;
+      kq = q - (nc - 1) * pf;
     }
     U.r = r;
     U.lo = P.sinks + r * m;
     U.hi = min(U.lo + m, U.n);
-    U.key0 = U.lo + kp * 2 * TILE_ROWS;
-    U.has1 = (U.key0 + TILE_ROWS) < U.hi;
-    U.nT = (P.G * nq_of(P, ai, r) + TILE_ROWS - 1) / TILE_ROWS;
+    U.key0 = U.lo + kq * span;
+    U.ntile = min(NA, (U.hi - U.key0 + TILE_ROWS - 1) / TILE_ROWS);
+    U.nT = (P.G * nq_of(P, ai, r) + Cfg<2>::BN - 1) / Cfg<2>::BN;
     U.R0 = U.R1 = U.ra = U.rb = U.nK = 0;
   }
   return U;
@@ -168,20 +246,21 @@ struct TileRef {
   int kind, t0, chunk;
 };
 __device__ __forceinline__ TileRef tile_at1(const KParams& P, const Unit& U, int i) {
+  constexpr int BN = Cfg<1>::BN;
   TileRef t;
   if (i < U.nK) {
     t.kind = 0;
-    t.t0 = i * TILE_ROWS;
+    t.t0 = i * BN;
     t.chunk = -1;
     return t;
   }
   i -= U.nK;
   for (int r = U.ra; r <= U.rb; ++r) {
-    if (!chunk_has_rows<1>(P, U.ai, r, U.R0, U.R1)) continue;
-    const int na = (nq_of(P, U.ai, r) + TILE_ROWS - 1) / TILE_ROWS;
+    if (!chunk_has_rows(P, U.ai, r, U.R0, U.R1)) continue;
+    const int na = (nq_of(P, U.ai, r) + BN - 1) / BN;
     if (i < na) {
       t.kind = 1;
-      t.t0 = i * TILE_ROWS;
+      t.t0 = i * BN;
       t.chunk = r;
       return t;
     }
@@ -196,35 +275,91 @@ __device__ __forceinline__ TileRef tile_at1(const KParams& P, const Unit& U, int
 // ----------------------------------------------------------------- kernel
 struct __align__(8) Bars {
   uint64_t a_full[2], a_empty[2];
-  uint64_t b_full[KSTAGES], b_empty[KSTAGES];
-  uint64_t d_full[2], d_empty[2];
+  uint64_t b_full[MAX_KST], b_empty[MAX_KST];
+  uint64_t d_full[4], d_empty[4];  // per (accumulator buffer, A tile)
+  uint64_t comb_full[2], comb_empty[2];  // pass 1: hand-off of the second column half per A tile
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
+// Online log-sum-exp update of one row over `N` fp32 logits (already in
+// registers) of which the first `lim` are visible.
+template <int N>
+__device__ __forceinline__ void lse_update(float (&v)[N], int lim, float c, float& mrun, float& ssum) {
+  if (lim <= 0) return;
+  if (lim < N) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = (k < lim) ? v[k] : -INFINITY;
+  }
+  // tile max: 8 independent chains, then a tree
+  float t[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    float a = v[q];
+#pragma unroll
+    for (int k = q + 8; k + 8 < N; k += 16) a = fmax3(a, v[k], v[k + 8]);
+    if ((N / 8) % 2 == 0) a = fmaxf(a, v[N - 8 + q]);
+    t[q] = a;
+  }
+  const float bm = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+  const float mn = fmaxf(mrun, bm * c);
+  ssum *= ex2(mrun - mn);  // 0 while nothing has been seen (mrun = -inf)
+  mrun = mn;
+  // sum of 2^(v*c - max): packed fp32 FMA/ADD, 4 packed partial sums
+  const uint64_t cc = pack2(c, c), nm = pack2(-mn, -mn);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) {
+    float x0, x1;
+    unpack2(fma2(pack2(v[2 * k], v[2 * k + 1]), cc, nm), x0, x1);
+    const uint64_t e = (k < EMU_PAIRS) ? exp2_poly2(x0, x1) : pack2(ex2(x0), ex2(x1));
+    acc[k & 3] = add2(acc[k & 3], e);
+  }
+  const uint64_t s2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+  float s0, s1;
+  unpack2(s2, s0, s1);
+  ssum += s0 + s1;
+}
+
 template <int PASS>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(kThreads<PASS>, 1)
     recon_kernel(const __grid_constant__ CUtensorMap tmQg, const __grid_constant__ CUtensorMap tmK0,
                  const __grid_constant__ CUtensorMap tmK1, const __grid_constant__ CUtensorMap tmApp,
                  const __grid_constant__ KParams P) {
+  constexpr int NA = Cfg<PASS>::NA, ABUF = Cfg<PASS>::ABUF, DBUF = Cfg<PASS>::DBUF;
+  constexpr int BN = Cfg<PASS>::BN, CSPLIT = Cfg<PASS>::CSPLIT, KST = Cfg<PASS>::KST;
+  constexpr int NCW = 4 * NA * CSPLIT;             // consumer warps
+  constexpr int BSTAGE = kBStage<PASS>;            // bytes of one B tile
+  constexpr int BHALF = BSTAGE / 2;                // one 64-column swizzled half of a B tile
+  constexpr int AHALF = TILE_BYTES / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                              // [2 buffers][2 tiles]
-  uint8_t* sB = smem + 4 * TILE_BYTES;             // [KSTAGES]
-  Bars* bars = reinterpret_cast<Bars*>(smem + SMEM_TILES * TILE_BYTES);
+  uint8_t* sA = smem;                              // [ABUF][NA] tiles
+  uint8_t* sB = smem + kABytes<PASS>;              // [KST] tiles of BN rows
+  float* sL = reinterpret_cast<float*>(sB + KST * BSTAGE);                      // [KST][128] (pass 2)
+  float2* sComb = reinterpret_cast<float2*>(sB + KST * (BSTAGE + LSE_STAGE_BYTES));  // [NA][128] (pass 1)
+  Bars* bars = reinterpret_cast<Bars*>(sB + KST * (BSTAGE + LSE_STAGE_BYTES) + kCombBytes<PASS>);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < ABUF; ++i) {
       mbar_init(&bars->a_full[i], 1);
       mbar_init(&bars->a_empty[i], 1);
-      mbar_init(&bars->d_full[i], 1);
-      mbar_init(&bars->d_empty[i], 8);
     }
-    for (int i = 0; i < KSTAGES; ++i) {
+    for (int i = 0; i < DBUF * NA; ++i) {
+      mbar_init(&bars->d_full[i], 1);
+      mbar_init(&bars->d_empty[i], 4 * CSPLIT);  // the warps reading this accumulator
+    }
+    for (int i = 0; i < KST; ++i) {
       mbar_init(&bars->b_full[i], 1);
-      mbar_init(&bars->b_empty[i], 1);
+      // pass 2: a stage also holds the B tile's lse2 row, which the consumer
+      // warps read after the MMA has finished with the tile
+      mbar_init(&bars->b_empty[i], PASS == 2 ? 1 + NCW : 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->comb_full[i], 4);
+      mbar_init(&bars->comb_empty[i], 4);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -239,10 +374,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
-  auto fail = [&](int where) {
+  auto fail = [&]() {
     *abort_flag = 1;
     record_status(P.status, DEV_TIMEOUT);
-    (void)where;
   };
 
   if (warp == 0) {
@@ -254,16 +388,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&tmApp);
       int s = 0, ab = 0;
       uint32_t bph = 0, aph = 0;
-      int issued_b[KSTAGES] = {};
+      int issued_b[MAX_KST] = {};
       int issued_a[2] = {0, 0};
       for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
         const Unit U = decode_unit<PASS>(P, u);
-        // A tiles
-        if (!mbar_wait(&bars->a_empty[ab], aph ^ 1, P.limit_ns)) { fail(1); break; }
-        const uint32_t abytes = (1 + U.has1) * TILE_BYTES;
-        mbar_arrive_expect_tx(&bars->a_full[ab], abytes);
-        for (int t = 0; t <= U.has1; ++t) {
-          uint8_t* dst = sA + (ab * 2 + t) * TILE_BYTES;
+        // A tiles (128 rows each; pass 2 reads them through the 128-row K maps)
+        if (!mbar_wait(&bars->a_empty[ab], aph ^ 1, P.limit_ns)) { fail(); break; }
+        mbar_arrive_expect_tx(&bars->a_full[ab], U.ntile * TILE_BYTES);
+        for (int t = 0; t < U.ntile; ++t) {
+          uint8_t* dst = sA + (ab * NA + t) * TILE_BYTES;
           const CUtensorMap* map;
           int32_t y;
           if (PASS == 1) {
@@ -274,15 +407,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             y = static_cast<int32_t>(U.lh * P.ldK + U.key0 + t * TILE_ROWS);
           }
           tma_load_2d(dst, map, 0, y, &bars->a_full[ab]);
-          tma_load_2d(dst + HALF_BYTES, map, 64, y, &bars->a_full[ab]);
+          tma_load_2d(dst + AHALF, map, 64, y, &bars->a_full[ab]);
         }
         issued_a[ab]++;
-        if (++ab == 2) { ab = 0; aph ^= 1; }
-        // B tiles
+        if (++ab == ABUF) { ab = 0; aph ^= 1; }
+        // B tiles (BN rows each)
         for (int i = 0; i < U.nT; ++i) {
           if (*abort_flag) break;
-          if (!mbar_wait(&bars->b_empty[s], bph ^ 1, P.limit_ns)) { fail(2); break; }
-          mbar_arrive_expect_tx(&bars->b_full[s], TILE_BYTES);
+          if (!mbar_wait(&bars->b_empty[s], bph ^ 1, P.limit_ns)) { fail(); break; }
+          mbar_arrive_expect_tx(&bars->b_full[s], PASS == 2 ? BSTAGE + LSE_STAGE_BYTES : BSTAGE);
           const CUtensorMap* map;
           int32_t y;
           if (PASS == 1) {
@@ -296,54 +429,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           } else {
             map = &tmQg;
-            y = U.lh * P.Rpad + U.r * P.CR + i * TILE_ROWS;
+            y = U.lh * P.Rpad + U.r * P.CR + i * BN;
+            bulk_load(sL + s * 128, P.lse2 + y, LSE_STAGE_BYTES, &bars->b_full[s]);
           }
-          uint8_t* dst = sB + s * TILE_BYTES;
+          uint8_t* dst = sB + s * BSTAGE;
           tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
-          tma_load_2d(dst + HALF_BYTES, map, 64, y, &bars->b_full[s]);
+          tma_load_2d(dst + BHALF, map, 64, y, &bars->b_full[s]);
           issued_b[s]++;
-          if (++s == KSTAGES) { s = 0; bph ^= 1; }
+          if (++s == KST) { s = 0; bph ^= 1; }
         }
       }
       // Wait for every copy this thread started (normally already consumed).
-      for (int i = 0; i < KSTAGES; ++i)
+      for (int i = 0; i < KST; ++i)
         if (issued_b[i] > 0) mbar_wait(&bars->b_full[i], (issued_b[i] - 1) & 1, P.limit_ns);
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < ABUF; ++i)
         if (issued_a[i] > 0) mbar_wait(&bars->a_full[i], (issued_a[i] - 1) & 1, P.limit_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, TILE_ROWS);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
       int s = 0, ab = 0, db = 0;
       uint32_t bph = 0, aph = 0, dph = 0;
       for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
         const Unit U = decode_unit<PASS>(P, u);
-        if (!mbar_wait(&bars->a_full[ab], aph, P.limit_ns)) { fail(3); break; }
+        if (!mbar_wait(&bars->a_full[ab], aph, P.limit_ns)) { fail(); break; }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + (ab * 2) * TILE_BYTES);
+        const uint32_t a0 = smem_u32(sA + (ab * NA) * TILE_BYTES);
         for (int i = 0; i < U.nT; ++i) {
           if (*abort_flag) break;
-          if (!mbar_wait(&bars->b_full[s], bph, P.limit_ns)) { fail(4); break; }
-          if (!mbar_wait(&bars->d_empty[db], dph ^ 1, P.limit_ns)) { fail(5); break; }
-          tc_fence_after();
-          const uint32_t b0 = smem_u32(sB + s * TILE_BYTES);
-          for (int t = 0; t <= U.has1; ++t) {
-            const uint32_t d = tbase + db * 256 + t * 128;
-            const uint32_t at = a0 + t * TILE_BYTES;
+          if (!mbar_wait(&bars->b_full[s], bph, P.limit_ns)) { fail(); break; }
+          const uint32_t b0 = smem_u32(sB + s * BSTAGE);
+          bool ok = true;
+          for (int t = 0; t < NA; ++t) {
+            uint64_t* de = &bars->d_empty[db * NA + t];
+            if (!mbar_wait(de, dph ^ 1, P.limit_ns)) { fail(); ok = false; break; }
+            tc_fence_after();
+            if (t < U.ntile) {
+              const uint32_t d = tbase + (db * NA + t) * BN;
+              const uint32_t at = a0 + t * TILE_BYTES;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t koff = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-              mma_bf16(d, sdesc_kmajor_sw128(at + koff), sdesc_kmajor_sw128(b0 + koff), idesc, k > 0 ? 1u : 0u);
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t ka = (k >> 2) * AHALF + (k & 3) * 32;
+                const uint32_t kb = (k >> 2) * BHALF + (k & 3) * 32;
+                mma_bf16(d, sdesc_kmajor_sw128(at + ka), sdesc_kmajor_sw128(b0 + kb), idesc, k > 0 ? 1u : 0u);
+              }
             }
+            // accumulator t of this tile is complete (missing tiles commit nothing new)
+            mma_commit(&bars->d_full[db * NA + t]);
           }
+          if (!ok) break;
           mma_commit(&bars->b_empty[s]);
-          mma_commit(&bars->d_full[db]);
-          if (++s == KSTAGES) { s = 0; bph ^= 1; }
-          if (++db == 2) { db = 0; dph ^= 1; }
+          if (++s == KST) { s = 0; bph ^= 1; }
+          if (++db == DBUF) { db = 0; dph ^= 1; }
         }
         mma_commit(&bars->a_empty[ab]);
-        if (++ab == 2) { ab = 0; aph ^= 1; }
+        if (++ab == ABUF) { ab = 0; aph ^= 1; }
       }
       // All issued MMAs must finish before TMEM is released.
       mma_commit(&bars->drain);
@@ -351,19 +492,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ consumers
-    const int wg = (warp - 2) >> 2;          // which A tile (accumulator)
+    // consumer warps come in groups of 4 (one per TMEM lane quarter); group
+    // `slot` reads accumulator wg = slot / CSPLIT, column part chalf
+    const int slot = (warp - 2) >> 2;
+    const int wg = slot / CSPLIT;            // which A tile (accumulator)
+    const int chalf = slot % CSPLIT;         // which part of the accumulator's columns
     const int quarter = warp & 3;            // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;     // row of the A tile
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + wg * 128;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c = P.scale_log2;
     int db = 0;
     uint32_t dph = 0;
+    uint32_t comb_ph = 0;  // pass 1: phase of the per-unit half-row hand-off
+    int cs = 0;            // pass 2: B stage of the next tile (same order as the MMA warp)
+    uint32_t cph = 0;
     for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
       const Unit U = decode_unit<PASS>(P, u);
+      const bool has_tile = wg < U.ntile;
       if (PASS == 1) {
         // ---- row LSE over the cache and the chunk's appended keys
         const int R = U.R0 + wg * TILE_ROWS + row;
-        const bool has_tile = (wg == 0) || U.has1;
         const int nc = P.n_chunks[U.ai];
         const int rr = min(R / P.CR, nc - 1);
         const int local = R - rr * P.CR;
@@ -372,47 +520,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int g = valid ? local / nq : 0;
         const int j = valid ? local - g * nq : 0;
         float mrun = -INFINITY, ssum = 0.f;
+        constexpr int COLS = BN / CSPLIT;  // columns of the tile this warp reads
+        static_assert(COLS == 128, "pass-1 consumers read 128 columns per tile");
         for (int i = 0; i < U.nT; ++i) {
-          if (!mbar_wait(&bars->d_full[db], dph, P.limit_ns)) { fail(6); break; }
+          uint64_t* df = &bars->d_full[db * NA + wg];
+          if (!mbar_wait(df, dph, P.limit_ns)) { fail(); break; }
           tc_fence_after();
           const TileRef tr = tile_at1(P, U, i);
-          int lim;
-          if (tr.kind == 0) lim = U.n - tr.t0;
-          else lim = (tr.chunk == rr) ? (j - tr.t0 + 1) : 0;
-#pragma unroll 1
-          for (int cb = 0; cb < 4; ++cb) {
-            float v[32];
+          const int lim = ((tr.kind == 0) ? U.n - tr.t0 : ((tr.chunk == rr) ? (j - tr.t0 + 1) : 0)) -
+                          chalf * COLS;
+          const uint32_t col = lane_addr + (db * NA + wg) * BN + chalf * COLS;
+          // two 64-column blocks; the accumulator is handed back to the MMA
+          // warp right after the second block is in registers
+          {
+            float v[64];
             __syncwarp();
-            tmem_ld32(lane_addr + db * 256 + cb * 32, v);
-            const int l32 = lim - cb * 32;
-            if (l32 <= 0) continue;
-            if (l32 < 32) {
-#pragma unroll
-              for (int k = 0; k < 32; ++k) v[k] = (k < l32) ? v[k] : -INFINITY;
-            }
-            float bm = v[0];
-#pragma unroll
-            for (int k = 1; k < 32; ++k) bm = fmaxf(bm, v[k]);
-            const float mn = fmaxf(mrun, bm * c);
-            if (mn > mrun) {
-              ssum *= ex2(mrun - mn);
-              mrun = mn;
-            }
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              acc0 += ex2(fmaf(v[k], c, -mrun));
-              acc1 += ex2(fmaf(v[k + 1], c, -mrun));
-            }
-            ssum += acc0 + acc1;
+            tmem_ld64(col, v);
+            lse_update<64>(v, lim, c, mrun, ssum);
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->d_empty[db]);
-          if (++db == 2) { db = 0; dph ^= 1; }
+          {
+            float v[64];
+            __syncwarp();
+            tmem_ld64(col + 64, v);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
+            lse_update<64>(v, lim - 64, c, mrun, ssum);
+          }
+          if (++db == DBUF) { db = 0; dph ^= 1; }
         }
         if (*abort_flag) break;
-        if (has_tile && R < P.Rpad) {
+        if (CSPLIT > 1) {
+          // fold the other column half's (max, sum) of this row into chalf 0
+          if (chalf == 1) {
+            if (!mbar_wait(&bars->comb_empty[wg], comb_ph ^ 1, P.limit_ns)) { fail(); break; }
+            sComb[wg * TILE_ROWS + row] = make_float2(mrun, ssum);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->comb_full[wg]);
+          } else {
+            if (!mbar_wait(&bars->comb_full[wg], comb_ph, P.limit_ns)) { fail(); break; }
+            const float2 o = sComb[wg * TILE_ROWS + row];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->comb_empty[wg]);
+            const float m = fmaxf(mrun, o.x);
+            const float s0 = (mrun == -INFINITY) ? 0.f : ssum * ex2(mrun - m);
+            const float s1 = (o.x == -INFINITY) ? 0.f : o.y * ex2(o.x - m);
+            mrun = m;
+            ssum = s0 + s1;
+          }
+          comb_ph ^= 1;
+        }
+        if (chalf == 0 && has_tile && R < P.Rpad) {
           const int64_t o = static_cast<int64_t>(U.lh) * P.Rpad + R;
           if (valid) {
             const float l2 = mrun + lg2(ssum);
@@ -429,31 +587,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         // ---- column max over the chunk's queries for one key per thread
         const int pos = U.key0 + wg * TILE_ROWS + row;
-        const bool valid = ((wg == 0) || U.has1) && pos < U.hi;
-        const float* lrow = P.lse2 + static_cast<int64_t>(U.lh) * P.Rpad + U.r * P.CR;
+        const bool valid = has_tile && pos < U.hi;
         float vmax = -INFINITY;
+        const uint64_t cc = pack2(c, c);
         for (int i = 0; i < U.nT; ++i) {
-          if (!mbar_wait(&bars->d_full[db], dph, P.limit_ns)) { fail(7); break; }
+          uint64_t* df = &bars->d_full[db * NA + wg];
+          if (!mbar_wait(df, dph, P.limit_ns)) { fail(); break; }
           tc_fence_after();
-          const float4* lt = reinterpret_cast<const float4*>(lrow + i * TILE_ROWS);
-#pragma unroll 1
-          for (int cb = 0; cb < 4; ++cb) {
-            float v[32];
-            __syncwarp();
-            tmem_ld32(lane_addr + db * 256 + cb * 32, v);
-#pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
-              const float4 l = __ldg(lt + cb * 8 + k4);
-              vmax = fmaxf(vmax, fmaf(v[4 * k4 + 0], c, -l.x));
-              vmax = fmaxf(vmax, fmaf(v[4 * k4 + 1], c, -l.y));
-              vmax = fmaxf(vmax, fmaf(v[4 * k4 + 2], c, -l.z));
-              vmax = fmaxf(vmax, fmaf(v[4 * k4 + 3], c, -l.w));
-            }
-          }
+          float v[128];
+          __syncwarp();
+          tmem_ld128(lane_addr + (db * NA + wg) * BN, v);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->d_empty[db]);
-          if (++db == 2) { db = 0; dph ^= 1; }
+          if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
+          if (++db == DBUF) { db = 0; dph ^= 1; }
+          // the tile's lse2 row arrived with the B tile (already complete
+          // when the MMA ran; this acquires it for this warp)
+          if (!mbar_wait(&bars->b_full[cs], cph, P.limit_ns)) { fail(); break; }
+          const float4* l4 = reinterpret_cast<const float4*>(sL + cs * TILE_ROWS);
+          float t[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) t[q] = -INFINITY;
+#pragma unroll
+          for (int k4 = 0; k4 < 32; ++k4) {
+            const float4 l = l4[k4];
+            float x0, x1, x2, x3;
+            unpack2(fma2(pack2(v[4 * k4], v[4 * k4 + 1]), cc, pack2(-l.x, -l.y)), x0, x1);
+            unpack2(fma2(pack2(v[4 * k4 + 2], v[4 * k4 + 3]), cc, pack2(-l.z, -l.w)), x2, x3);
+            t[(2 * k4) & 7] = fmax3(t[(2 * k4) & 7], x0, x1);
+            t[(2 * k4 + 1) & 7] = fmax3(t[(2 * k4 + 1) & 7], x2, x3);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->b_empty[cs]);
+          if (++cs == KST) { cs = 0; cph ^= 1; }
+          vmax = fmax3(vmax, fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]));
+          vmax = fmax3(vmax, t[6], t[7]);
         }
         if (*abort_flag) break;
         if (valid) P.score[static_cast<int64_t>(U.lh) * P.ldS + pos] = ex2(vmax);
@@ -471,7 +639,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ----------------------------------------------------------------- gather
 // Fill the row space Qg (query rows, zero padding) and, for KV², the
-// appended keys Kg = K[l, h, sel].  Half a warp moves one 256-byte row.
+// appended keys Kg = K[l, h, sel].  Half a warp moves one 256-byte row; each
+// half-warp has four rows in flight.
 struct GParams {
   int Hkv, Hq, G;
   int n_active;
@@ -490,59 +659,75 @@ struct GParams {
   int* status;
 };
 
+// Source and destination of gathered row w (src null: zero row).
+__device__ __forceinline__ void gather_row(const GParams& P, int64_t w, int64_t rows_q, const uint4*& src,
+                                           uint4*& dst) {
+  src = nullptr;
+  if (w < rows_q) {
+    const int64_t per = static_cast<int64_t>(P.Hkv) * P.Rpad;
+    const int ai = static_cast<int>(w / per);
+    const int64_t rem = w - ai * per;
+    const int h = static_cast<int>(rem / P.Rpad);
+    const int R = static_cast<int>(rem - static_cast<int64_t>(h) * P.Rpad);
+    const int layer = P.layer[ai];
+    const int nc = P.n_chunks[ai];
+    const int r = min(R / P.CR, nc - 1);
+    const int local = R - r * P.CR;
+    const int nq = (r == nc - 1) ? P.nq_last : P.nq_full;
+    dst = reinterpret_cast<uint4*>(P.Qg + ((static_cast<int64_t>(layer) * P.Hkv + h) * P.Rpad + R) * kHeadDim);
+    if (local < P.G * nq) {
+      const int g = local / nq, j = local - g * nq;
+      const int t = r * P.nq_full + j;
+      const int s = P.sel ? P.sel[t] : t;
+      if (s >= 0 && s < P.ldQ)
+        src = reinterpret_cast<const uint4*>(
+            P.Qsrc + ((static_cast<int64_t>(layer) * P.Hq + h * P.G + g) * P.ldQ + s) * kHeadDim);
+      else if ((threadIdx.x & 15) == 0)
+        record_status(P.status, DEV_BOUNDS);
+    }
+  } else {
+    const int64_t w2 = w - rows_q;
+    const int64_t per = static_cast<int64_t>(P.Hkv) * P.Q;
+    const int ai = static_cast<int>(w2 / per);
+    const int64_t rem = w2 - ai * per;
+    const int h = static_cast<int>(rem / P.Q);
+    const int t = static_cast<int>(rem - static_cast<int64_t>(h) * P.Q);
+    const int layer = P.layer[ai];
+    dst = reinterpret_cast<uint4*>(P.Kg + ((static_cast<int64_t>(layer) * P.Hkv + h) * P.Q + t) * kHeadDim);
+    const int s = P.sel ? P.sel[t] : t;
+    if (s >= 0 && s < P.n[ai])
+      src = reinterpret_cast<const uint4*>(P.K[P.slab[ai]] +
+                                           ((static_cast<int64_t>(layer) * P.Hkv + h) * P.ldK + s) * kHeadDim);
+    else if ((threadIdx.x & 15) == 0)
+      record_status(P.status, DEV_BOUNDS);
+  }
+}
+
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GParams P) {
+  constexpr int ROWS = 4;
   const int64_t rows_q = static_cast<int64_t>(P.n_active) * P.Hkv * P.Rpad;
   const int64_t rows_k = P.Kg ? static_cast<int64_t>(P.n_active) * P.Hkv * P.Q : 0;
   const int64_t total = rows_q + rows_k;
   const int sub = threadIdx.x & 15;
+  const int64_t hw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 4);
-  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4); w < total;
-       w += stride) {
-    uint4 val = make_uint4(0, 0, 0, 0);
-    __nv_bfloat16* dst;
-    if (w < rows_q) {
-      const int64_t per = static_cast<int64_t>(P.Hkv) * P.Rpad;
-      const int ai = static_cast<int>(w / per);
-      const int64_t rem = w - ai * per;
-      const int h = static_cast<int>(rem / P.Rpad);
-      const int R = static_cast<int>(rem - static_cast<int64_t>(h) * P.Rpad);
-      const int layer = P.layer[ai];
-      const int nc = P.n_chunks[ai];
-      const int r = min(R / P.CR, nc - 1);
-      const int local = R - r * P.CR;
-      const int nq = (r == nc - 1) ? P.nq_last : P.nq_full;
-      dst = P.Qg + ((static_cast<int64_t>(layer) * P.Hkv + h) * P.Rpad + R) * kHeadDim;
-      if (local < P.G * nq) {
-        const int g = local / nq, j = local - g * nq;
-        const int t = r * P.nq_full + j;
-        const int src = P.sel ? P.sel[t] : t;
-        if (src >= 0 && src < P.ldQ) {
-          const __nv_bfloat16* s =
-              P.Qsrc + ((static_cast<int64_t>(layer) * P.Hq + h * P.G + g) * P.ldQ + src) * kHeadDim;
-          val = __ldg(reinterpret_cast<const uint4*>(s) + sub);
-        } else if (sub == 0) {
-          record_status(P.status, DEV_BOUNDS);
-        }
-      }
-    } else {
-      const int64_t w2 = w - rows_q;
-      const int64_t per = static_cast<int64_t>(P.Hkv) * P.Q;
-      const int ai = static_cast<int>(w2 / per);
-      const int64_t rem = w2 - ai * per;
-      const int h = static_cast<int>(rem / P.Q);
-      const int t = static_cast<int>(rem - static_cast<int64_t>(h) * P.Q);
-      const int layer = P.layer[ai];
-      dst = P.Kg + ((static_cast<int64_t>(layer) * P.Hkv + h) * P.Q + t) * kHeadDim;
-      const int src = P.sel ? P.sel[t] : t;
-      if (src >= 0 && src < P.n[ai]) {
-        const __nv_bfloat16* s =
-            P.K[P.slab[ai]] + ((static_cast<int64_t>(layer) * P.Hkv + h) * P.ldK + src) * kHeadDim;
-        val = __ldg(reinterpret_cast<const uint4*>(s) + sub);
-      } else if (sub == 0) {
-        record_status(P.status, DEV_BOUNDS);
+  for (int64_t w0 = hw; w0 < total; w0 += stride * ROWS) {
+    uint4 val[ROWS];
+    uint4* dst[ROWS];
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u) {
+      const int64_t w = w0 + u * stride;
+      dst[u] = nullptr;
+      val[u] = make_uint4(0, 0, 0, 0);
+      if (w < total) {
+        const uint4* src;
+        gather_row(P, w, rows_q, src, dst[u]);
+        if (src) val[u] = __ldg(src + sub);
       }
     }
-    reinterpret_cast<uint4*>(dst)[sub] = val;
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u)
+      if (dst[u]) dst[u][sub] = val[u];
   }
 }
 
@@ -559,9 +744,9 @@ size_t recon_ws_bytes(int L, int Hkv, int G, int n_chunks, int nq_full, int nq_l
   const int64_t Rpad = recon_rows(G, n_chunks, nq_full, nq_last);
   size_t b = 0;
   auto add = [&](size_t bytes) { b = ((b + 255) & ~size_t(255)) + bytes; };
-  add(static_cast<size_t>(L) * Hkv * Rpad * kHeadDim * 2);      // Qg
+  add(static_cast<size_t>(L) * Hkv * Rpad * kHeadDim * 2);            // Qg
   if (need_kg) add(static_cast<size_t>(L) * Hkv * Q * kHeadDim * 2);  // Kg
-  add(static_cast<size_t>(L) * Hkv * Rpad * 4);                  // lse2
+  add(static_cast<size_t>(L) * Hkv * Rpad * 4);                        // lse2
   return b + 256;
 }
 
@@ -595,7 +780,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   gp.status = status_word();
   {
     const int64_t rows = static_cast<int64_t>(pr.n_active) * pr.Hkv * (Rpad + (gp.Kg ? pr.Q : 0));
-    int64_t blocks = (rows + 15) / 16;
+    int64_t blocks = (rows + 63) / 64;
     const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
@@ -609,25 +794,31 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
 
   // ---- tensor maps
   // Rows are addressed by model layer index, so the maps span all L layers.
-  CUtensorMap tmQg, tmK0, tmK1, tmApp;
+  // Pass 1 streams keys in B tiles of Cfg<1>::BN rows; pass 2 reads keys as
+  // 128-row A tiles and query rows as 128-row B tiles.
+  CUtensorMap tmQg, tmK0a, tmK1a, tmK0b, tmK1b, tmApp;
   const uint64_t LH = static_cast<uint64_t>(pr.L) * pr.Hkv;
+  const void* k1 = pr.K[1] ? pr.K[1] : pr.K[0];
   if (!make_tmap_rows(&tmQg, ws.Qg, LH * Rpad, TILE_ROWS)) return cudaErrorInvalidValue;
-  if (!make_tmap_rows(&tmK0, pr.K[0], LH * pr.ldK, TILE_ROWS)) return cudaErrorInvalidValue;
-  if (!make_tmap_rows(&tmK1, pr.K[1] ? pr.K[1] : pr.K[0], LH * pr.ldK, TILE_ROWS)) return cudaErrorInvalidValue;
+  if (!make_tmap_rows(&tmK0a, pr.K[0], LH * pr.ldK, TILE_ROWS)) return cudaErrorInvalidValue;
+  if (!make_tmap_rows(&tmK1a, k1, LH * pr.ldK, TILE_ROWS)) return cudaErrorInvalidValue;
+  if (!make_tmap_rows(&tmK0b, pr.K[0], LH * pr.ldK, Cfg<1>::BN)) return cudaErrorInvalidValue;
+  if (!make_tmap_rows(&tmK1b, k1, LH * pr.ldK, Cfg<1>::BN)) return cudaErrorInvalidValue;
   const void* app = pr.Kapp ? pr.Kapp : ws.Kg;
   const int64_t ldApp = pr.Kapp ? pr.ldApp : pr.Q;
-  if (!make_tmap_rows(&tmApp, app, LH * ldApp, TILE_ROWS)) return cudaErrorInvalidValue;
+  if (!make_tmap_rows(&tmApp, app, LH * ldApp, Cfg<1>::BN)) return cudaErrorInvalidValue;
 
   KParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.Hkv = pr.Hkv; kp.Hq = pr.Hq; kp.G = G; kp.sinks = pr.sinks; kp.n_active = pr.n_active;
+  constexpr int span2 = Cfg<2>::NA * TILE_ROWS;
   int acc = 0;
   for (int a = 0; a < pr.n_active; ++a) {
     const ReconLayer& ly = pr.lay[a];
     kp.layer[a] = ly.layer; kp.n[a] = ly.n; kp.m[a] = ly.m; kp.n_chunks[a] = ly.n_chunks;
     kp.last_len[a] = ly.last_len; kp.slab[a] = ly.slab;
     kp.unit_off[a] = acc;
-    const int pf = (ly.m + 255) / 256, pl = (ly.last_len + 255) / 256;
+    const int pf = (ly.m + span2 - 1) / span2, pl = (ly.last_len + span2 - 1) / span2;
     acc += pr.Hkv * ((ly.n_chunks - 1) * pf + pl);
   }
   kp.unit_off[pr.n_active] = acc;
@@ -635,7 +826,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   kp.nq_full = pr.nq_full; kp.nq_last = pr.nq_last; kp.Q = pr.Q;
   kp.CR = CR; kp.Rpad = Rpad;
   kp.ldApp = static_cast<int32_t>(ldApp);
-  kp.pairs1 = (Rpad + 255) / 256;
+  kp.units1 = (Rpad + Cfg<1>::NA * TILE_ROWS - 1) / (Cfg<1>::NA * TILE_ROWS);
   kp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
   kp.lse2 = ws.lse2;
   kp.lse_out = pr.lse_out;
@@ -644,16 +835,17 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   kp.status = status_word();
   kp.limit_ns = wait_limit_ns();
 
-  cudaError_t ea = cudaFuncSetAttribute(recon_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t ea = cudaFuncSetAttribute(recon_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes<1>);
   if (ea != cudaSuccess) return ea;
-  ea = cudaFuncSetAttribute(recon_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  ea = cudaFuncSetAttribute(recon_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes<2>);
   if (ea != cudaSuccess) return ea;
   const int sms = num_sms();
   // pass 1
-  kp.n_units = pr.n_active * pr.Hkv * kp.pairs1;
+  kp.n_units = pr.n_active * pr.Hkv * kp.units1;
   if (kp.n_units > 0) {
     ProfScope ps("recon_lse", st);
-    recon_kernel<1><<<kp.n_units < sms ? kp.n_units : sms, NUM_THREADS, SMEM_BYTES, st>>>(tmQg, tmK0, tmK1, tmApp, kp);
+    recon_kernel<1><<<kp.n_units < sms ? kp.n_units : sms, kThreads<1>, kSmemBytes<1>, st>>>(tmQg, tmK0b, tmK1b,
+                                                                                            tmApp, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -661,7 +853,8 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   kp.n_units = acc;
   if (kp.n_units > 0) {
     ProfScope ps("recon_colmax", st);
-    recon_kernel<2><<<kp.n_units < sms ? kp.n_units : sms, NUM_THREADS, SMEM_BYTES, st>>>(tmQg, tmK0, tmK1, tmApp, kp);
+    recon_kernel<2><<<kp.n_units < sms ? kp.n_units : sms, kThreads<2>, kSmemBytes<2>, st>>>(tmQg, tmK0a, tmK1a,
+                                                                                            tmApp, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
