@@ -24,7 +24,13 @@
  * Memory     The caller owns every buffer (device memory unless stated as
  *            host), including the workspace; the library never allocates or
  *            frees memory.  Pointers must be 16-byte aligned; the workspace
- *            must be 256-byte aligned.
+ *            must be 256-byte aligned.  Exception: the query pool Qpool
+ *            (kvc_recon_score, kvc_compress) and the sources K, V of
+ *            kvc_compact and V of kvc_compress may also be page-locked host
+ *            memory mapped into the device address space (cudaHostAlloc, or
+ *            cudaHostRegister with mapping); the kernels then read only the
+ *            selected query rows and the kept K/V rows, each once, across
+ *            the host link (NVLink-C2C on Grace-Blackwell).
  * Streams    All device work is enqueued on `stream` (NULL = legacy default
  *            stream) and is asynchronous; host-side outputs are written
  *            before the call returns.

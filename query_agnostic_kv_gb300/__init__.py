@@ -138,6 +138,21 @@ def _dev(t, dtype=None, name="tensor"):
     return c_vp(t.data_ptr())
 
 
+def _dev_or_pinned(t, dtype=None, name="tensor"):
+    """Like _dev, but also accepts a pinned (page-locked) host tensor, which
+    is mapped into the device address space: kernels then read only the rows
+    they need across the host link instead of a full copy."""
+    if t is not None and isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise TypeError(f"{name} must be a CUDA tensor or a pinned host tensor")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return c_vp(t.data_ptr())
+    return _dev(t, dtype, name)
+
+
 def _ws(ws):
     if ws is None:
         return None, 0
@@ -243,7 +258,7 @@ def kvc_select_queries(N, sinks, m, rho, p, sel, stream=None) -> None:
 def kvc_recon_score(shape, K, Qpool, sel, sinks, m, rho, score, Kapp=None, lse=None, ws=None, stream=None) -> None:
     w, wb = _ws(ws)
     _check("kvc_recon_score", lib().kvc_recon_score(
-        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev(Qpool, torch.bfloat16, "Qpool"),
+        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"),
         _dev(sel, torch.int32, "sel"), sinks, m, float(rho), _dev(Kapp, torch.bfloat16, "Kapp"),
         _dev(score, torch.float32, "score"), _dev(lse, torch.float32, "lse"), w, wb, _stream(stream)))
 
@@ -261,8 +276,8 @@ def kvc_evict_topk(shape, score, sinks, k_per_layer, kept, ws=None, stream=None)
 
 
 def kvc_compact(shape, K, V, kept, k_per_layer, Kc, Vc, stream=None) -> None:
-    _check("kvc_compact", lib().kvc_compact(_shape(shape), _dev(K, torch.bfloat16, "K"),
-                                            _dev(V, torch.bfloat16, "V"), _dev(kept, torch.int32, "kept"),
+    _check("kvc_compact", lib().kvc_compact(_shape(shape), _dev_or_pinned(K, torch.bfloat16, "K"),
+                                            _dev_or_pinned(V, torch.bfloat16, "V"), _dev(kept, torch.int32, "kept"),
                                             _i32_array(k_per_layer), _dev(Kc, torch.bfloat16, "Kc"),
                                             _dev(Vc, torch.bfloat16, "Vc"), _stream(stream)))
 
@@ -271,8 +286,8 @@ def kvc_compress(shape, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, K
                  score=None, ws=None, stream=None) -> None:
     w, wb = _ws(ws)
     _check("kvc_compress", lib().kvc_compress(
-        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev(V, torch.bfloat16, "V"),
-        _dev(Qpool, torch.bfloat16, "Qpool"), sinks, m, float(rho), passes, _i32_array(k_per_layer),
+        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(V, torch.bfloat16, "V"),
+        _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"), sinks, m, float(rho), passes, _i32_array(k_per_layer),
         _dev(kept, torch.int32, "kept"), _dev(Kc, torch.bfloat16, "Kc"), _dev(Vc, torch.bfloat16, "Vc"),
         _dev(p, torch.float32, "p"), _dev(sel, torch.int32, "sel"), _dev(score, torch.float32, "score"), w, wb,
         _stream(stream)))

@@ -135,7 +135,10 @@ constexpr float EXP2_C1 = 0.6932609677314758f;
 constexpr float EXP2_C2 = 0.2426111251115799f;
 constexpr float EXP2_C3 = 0.0551716685295105f;
 constexpr float ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23
-constexpr int EMU_PAIRS = 0;                // column pairs (of 32 per 64-column half) on the FMA pipe
+#ifndef KVC_EMU_PAIRS
+#define KVC_EMU_PAIRS 0
+#endif
+constexpr int EMU_PAIRS = KVC_EMU_PAIRS;                // column pairs (of 32 per 64-column half) on the FMA pipe
 
 __device__ __forceinline__ uint64_t exp2_poly2(float x0, float x1) {
   x0 = fmaxf(x0, -125.0f);
@@ -320,6 +323,74 @@ __device__ __forceinline__ void lse_update(float (&v)[N], int lim, float c, floa
   float s0, s1;
   unpack2(s2, s0, s1);
   ssum += s0 + s1;
+}
+
+// Sum of 2^(v*c - m) over N logits (masked entries are -inf and add 0).
+template <int N>
+__device__ __forceinline__ float exp2_sum(const float (&v)[N], float c, float m) {
+  const uint64_t cc = pack2(c, c), nm = pack2(-m, -m);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) {
+    float x0, x1;
+    unpack2(fma2(pack2(v[2 * k], v[2 * k + 1]), cc, nm), x0, x1);
+    const uint64_t e = (k < EMU_PAIRS) ? exp2_poly2(x0, x1) : pack2(ex2(x0), ex2(x1));
+    acc[k & 3] = add2(acc[k & 3], e);
+  }
+  const uint64_t s2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+  float s0, s1;
+  unpack2(s2, s0, s1);
+  return s0 + s1;
+}
+
+template <int N>
+__device__ __forceinline__ float block_max(const float (&v)[N]) {
+  float t[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    float a = v[q];
+#pragma unroll
+    for (int k = q + 8; k + 8 < N; k += 16) a = fmax3(a, v[k], v[k + 8]);
+    if ((N / 8) % 2 == 0) a = fmaxf(a, v[N - 8 + q]);
+    t[q] = a;
+  }
+  return fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+}
+
+// Log-sum-exp update with a lazily moved reference: sum_i 2^(x_i - mref) is
+// exact for any reference, it only must not overflow.  The exact block max
+// is taken for the row's first visible block; afterwards each block is summed
+// against the current reference and only if that sum exceeds 2^40 (a logit
+// more than ~34 above the reference, i.e. overflow is possible) the block is
+// redone against its own max, with the running sum rescaled.  This drops the
+// per-element max from the common path.
+template <int N>
+__device__ __forceinline__ void lse_update_lazy(float (&v)[N], int lim, float c, float& mref, float& ssum) {
+  if (lim <= 0) return;
+  if (lim < N) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = (k < lim) ? v[k] : -INFINITY;
+  }
+  if (mref == -INFINITY) mref = block_max<N>(v) * c;  // first visible block of the row
+  float s = exp2_sum<N>(v, c, mref);
+  if (!(s <= 1099511627776.0f)) {  // 2^40, also catches inf / NaN
+    const float mn = fmaxf(mref, block_max<N>(v) * c);
+    ssum *= ex2(mref - mn);
+    mref = mn;
+    s = exp2_sum<N>(v, c, mref);
+  }
+  ssum += s;
+}
+
+#ifndef KVC_LAZY_MAX
+#define KVC_LAZY_MAX 1
+#endif
+template <int N>
+__device__ __forceinline__ void row_update(float (&v)[N], int lim, float c, float& m, float& s) {
+  if (KVC_LAZY_MAX)
+    lse_update_lazy<N>(v, lim, c, m, s);
+  else
+    lse_update<N>(v, lim, c, m, s);
 }
 
 template <int PASS>
@@ -536,7 +607,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
             float v[64];
             __syncwarp();
             tmem_ld64(col, v);
-            lse_update<64>(v, lim, c, mrun, ssum);
+            row_update<64>(v, lim, c, mrun, ssum);
           }
           {
             float v[64];
@@ -545,7 +616,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
-            lse_update<64>(v, lim - 64, c, mrun, ssum);
+            row_update<64>(v, lim - 64, c, mrun, ssum);
           }
           if (++db == DBUF) { db = 0; dph ^= 1; }
         }

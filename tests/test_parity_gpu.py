@@ -170,6 +170,32 @@ def test_compress_matches_stages_and_is_deterministic(qk):
     assert np.array_equal(res[0][0].reshape(L, H, k), stages["kept"])
 
 
+def test_pinned_host_pool_and_values(qk):
+    """The query pool and V may stay in pinned host memory (mapped into the
+    device address space): the outputs are bit-identical to the
+    device-resident run."""
+    cfg = CASES["ragged-1000"]
+    x = ks.gen_kv2(cfg)
+    L, H, Hq, N, S = cfg.L, cfg.Hkv, cfg.Hq, cfg.N, cfg.sinks
+    shape = (L, H, Hq, 128, N)
+    K, V, Q = to_dev(x.K), to_dev(x.V), to_dev(x.Q)
+    hV = torch.from_numpy(x.V.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hQ = torch.from_numpy(x.Q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    k = qk.kvc_budget_count(cfg.budget, N, S)
+    ws = torch.empty(qk.kvc_workspace_size(shape, S, cfg.m, cfg.rho), dtype=torch.uint8, device=DEV)
+    outs = []
+    for v_in, q_in in ((V, Q), (hV, hQ)):
+        kept = torch.empty(L * H * k, dtype=torch.int32, device=DEV)
+        Kc = torch.empty(L * H * k * 128, dtype=torch.bfloat16, device=DEV)
+        Vc = torch.empty_like(Kc)
+        score = torch.empty(L * H * N, dtype=torch.float32, device=DEV)
+        qk.kvc_compress(shape, K, v_in, q_in, S, cfg.m, cfg.rho, 1, [k] * L, kept, Kc, Vc, score=score, ws=ws)
+        assert qk.kvc_stream_status() == 0
+        outs.append((kept.cpu(), bits_of(Kc), bits_of(Vc), score.cpu()))
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(np.asarray(a), np.asarray(b))
+
+
 def test_refinement_passes(qk):
     """passes=3: each pass's mean stage-2 score replaces the proxy."""
     cfg = ks.scaled(ks.TINY, name="refine", L=2, Hkv=2, Hq=4, N=900, m=256, rho=0.25, budget=0.05,
