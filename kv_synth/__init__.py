@@ -45,12 +45,14 @@ NORM_SIGMA = 0.3
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (nearest even); return uint16 bit patterns."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    lsb = (u >> 16) & 1
-    r = (u + 0x7FFF + lsb) >> 16
-    # NaN stays NaN (not produced by these generators, kept for safety)
-    nan = np.isnan(x)
+    u = x.view(np.uint32)
+    # round to nearest even on the upper 16 bits; uint32 wrap-around only
+    # affects NaN patterns, which are handled separately
+    r = u + np.uint32(0x7FFF)
+    r += (u >> np.uint32(16)) & np.uint32(1)
+    r >>= np.uint32(16)
     out = r.astype(np.uint16)
+    nan = np.isnan(x)
     if nan.any():
         out[nan] = 0x7FC0
     return out

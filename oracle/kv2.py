@@ -316,6 +316,38 @@ def layer_budgets(sens, alpha: float, mean_budget: int, sinks: int) -> np.ndarra
     return np.maximum(base, sinks)
 
 
+def block_step_scores(Kc: np.ndarray, Qprompt: np.ndarray, Kprompt: np.ndarray, sinks: int) -> np.ndarray:
+    """Scores of every cache row of one layer against the episode prompt
+    (the KV² max rule with the prompt's queries appended causally, one chunk
+    covering all non-sink rows).  Kc: [Hkv, n, d]; returns [Hkv, n] with NaN
+    at the sinks."""
+    H, n, d = Kc.shape
+    G = Qprompt.shape[0] // H
+    P = Qprompt.shape[1]
+    chunks = [Chunk(sinks, n, 0, P)]
+    return np.stack([recon_head(Kc[h], Qprompt[h * G:(h + 1) * G], Kprompt[h], chunks)[0] for h in range(H)])
+
+
+def block_step(Kc, Vc, pos, Kb, Vb, t0, Qprompt, Kprompt, M, sinks):
+    """One block-prefill step of one layer: append the block (global
+    positions t0..), and if the cache then exceeds M rows, keep the M best
+    rows per KV head (sinks pinned, lower global position wins a tie) in
+    position order.  Returns (Kc, Vc, pos, scores or None)."""
+    H = Kb.shape[0]
+    B = Kb.shape[1]
+    Kc = np.concatenate([Kc, Kb], axis=1)
+    Vc = np.concatenate([Vc, Vb], axis=1)
+    pos = np.concatenate([pos, np.broadcast_to(np.arange(t0, t0 + B), (H, B))], axis=1)
+    n = Kc.shape[1]
+    if n <= M:
+        return Kc, Vc, pos, None
+    score = block_step_scores(Kc, Qprompt, Kprompt, sinks)
+    work = score[None].copy()
+    kept = evict(work, sinks, [M])[0]
+    return (np.stack([Kc[h][kept[h]] for h in range(H)]), np.stack([Vc[h][kept[h]] for h in range(H)]),
+            np.stack([pos[h][kept[h]] for h in range(H)]), score)
+
+
 def block_prefill_layer(Kh: np.ndarray, Vh: np.ndarray, Qprompt: np.ndarray, Kprompt: np.ndarray,
                         block: int, M: int, sinks: int, state=None, n_blocks=None):
     """EpiCache block prefill of one layer for one episode.
@@ -345,18 +377,7 @@ def block_prefill_layer(Kh: np.ndarray, Vh: np.ndarray, Qprompt: np.ndarray, Kpr
     done = 0
     while t0 < n_hist and (n_blocks is None or done < n_blocks):
         t1 = min(t0 + block, n_hist)
-        Kc = np.concatenate([Kc, Kh[:, t0:t1]], axis=1)
-        Vc = np.concatenate([Vc, Vh[:, t0:t1]], axis=1)
-        pos = np.concatenate([pos, np.broadcast_to(np.arange(t0, t1), (H, t1 - t0))], axis=1)
-        n = Kc.shape[1]
-        if n > M:
-            chunks = [Chunk(sinks, n, 0, P)]
-            score = np.stack([recon_head(Kc[h], Qprompt[h * G:(h + 1) * G], Kprompt[h], chunks)[0]
-                              for h in range(H)])
-            kept = evict(score[None], sinks, [M])[0]
-            Kc = np.stack([Kc[h][kept[h]] for h in range(H)])
-            Vc = np.stack([Vc[h][kept[h]] for h in range(H)])
-            pos = np.stack([pos[h][kept[h]] for h in range(H)])
+        Kc, Vc, pos, _ = block_step(Kc, Vc, pos, Kh[:, t0:t1], Vh[:, t0:t1], t0, Qprompt, Kprompt, M, sinks)
         t0 = t1
         done += 1
     return Kc, Vc, pos, t0
