@@ -224,4 +224,23 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// ---------------------------------------------------------------- A operand in TMEM
+// Copy one 128-row x 16-element (256-bit) K slice of a K-major operand from
+// shared memory (described like an MMA operand) into 8 TMEM columns: row r
+// goes to lane r, two bf16 per 32-bit column.  Asynchronous, ordered with the
+// issuing thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 }  // namespace kvc

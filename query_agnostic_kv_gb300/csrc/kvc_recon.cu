@@ -44,7 +44,7 @@ constexpr int TILE_ROWS = 128;                  // rows of an A tile (TMEM lanes
 constexpr int TILE_BYTES = TILE_ROWS * 256;     // 128 rows x 128 bf16
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int LSE_STAGE_BYTES = 128 * 4;        // pass 2: lse2 of the B tile's 128 query rows
-constexpr int MAX_KST = 3;
+constexpr int MAX_KST = 4;
 
 // Per-pass shape of the pipeline.  B tiles of 256 rows (MMA N = 256) halve
 // the A-operand re-reads from shared memory per FLOP; with N = 128 the
@@ -53,22 +53,28 @@ template <int PASS>
 struct Cfg;
 template <>
 struct Cfg<1> {
-  static constexpr int NA = 2;      // A tiles (128 query rows each) per unit
-  static constexpr int ABUF = 1;    // A buffers
-  static constexpr int DBUF = 1;    // accumulator buffers per A tile
-  static constexpr int BN = 256;    // rows (keys) of a B tile = MMA N
-  static constexpr int CSPLIT = 2;  // consumer warps sharing one TMEM lane quarter (column split)
-  static constexpr int KST = 2;     // B-tile ring depth
+  static constexpr int NA = 2;          // A tiles (128 query rows each) per unit
+  static constexpr int ABUF = 1;        // A buffers in shared memory
+  static constexpr int DBUF = 1;        // accumulator buffers per A tile
+  static constexpr int BN = 256;        // rows (keys) of a B tile = MMA N
+  static constexpr int CSPLIT = 2;      // consumer warps sharing one TMEM lane quarter (column split)
+  static constexpr int KST = 2;         // B-tile ring depth
+  static constexpr bool A_TMEM = false; // A read by the MMA from shared memory
 };
+// Pass 2 keeps its two key tiles in TMEM (copied from a shared-memory
+// staging buffer once per unit, double-buffered in TMEM), so every MMA reads
+// only the 128-row query tile from shared memory.
 template <>
 struct Cfg<2> {
   static constexpr int NA = 2;
-  static constexpr int ABUF = 2;
-  static constexpr int DBUF = 2;
+  static constexpr int ABUF = 1;
+  static constexpr int DBUF = 1;
   static constexpr int BN = 128;
   static constexpr int CSPLIT = 1;
-  static constexpr int KST = 3;
+  static constexpr int KST = 4;
+  static constexpr bool A_TMEM = true;
 };
+constexpr uint32_t TMEM_A_BASE = 256;  // pass 2: A buffers at TMEM columns [256, 512), 64 columns per tile
 template <int PASS>
 constexpr int kThreads = 64 + 128 * Cfg<PASS>::NA * Cfg<PASS>::CSPLIT;
 template <int PASS>
@@ -81,7 +87,8 @@ template <int PASS>
 constexpr int kSmemBytes = 1024 + kABytes<PASS> + Cfg<PASS>::KST * (kBStage<PASS> + LSE_STAGE_BYTES) +
                            kCombBytes<PASS> + 256;
 static_assert(Cfg<1>::NA * Cfg<1>::DBUF * Cfg<1>::BN <= TMEM_COLS, "TMEM pass 1");
-static_assert(Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_COLS, "TMEM pass 2");
+static_assert(Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_A_BASE && TMEM_A_BASE + 2 * Cfg<2>::NA * 64 <= TMEM_COLS,
+              "TMEM pass 2");
 static_assert(kSmemBytes<1> <= 232448 && kSmemBytes<2> <= 232448, "shared memory budget of one CTA");
 static_assert(Cfg<1>::KST <= MAX_KST && Cfg<2>::KST <= MAX_KST, "ring depth");
 
@@ -281,6 +288,7 @@ struct __align__(8) Bars {
   uint64_t b_full[MAX_KST], b_empty[MAX_KST];
   uint64_t d_full[4], d_empty[4];  // per (accumulator buffer, A tile)
   uint64_t comb_full[2], comb_empty[2];  // pass 1: hand-off of the second column half per A tile
+  uint64_t ta_free[2];                   // pass 2: TMEM A buffer no longer read by the MMAs
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -431,6 +439,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->comb_full[i], 4);
       mbar_init(&bars->comb_empty[i], 4);
+      mbar_init(&bars->ta_free[i], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
@@ -520,13 +529,31 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      constexpr bool ATM = Cfg<PASS>::A_TMEM;
       int s = 0, ab = 0, db = 0;
       uint32_t bph = 0, aph = 0, dph = 0;
+      int tb = 0;                          // TMEM A buffer (A_TMEM passes)
+      uint32_t ta_ph[2] = {0u, 0u};
+      int ta_used[2] = {0, 0};
       for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
         const Unit U = decode_unit<PASS>(P, u);
         if (!mbar_wait(&bars->a_full[ab], aph, P.limit_ns)) { fail(); break; }
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA + (ab * NA) * TILE_BYTES);
+        const uint32_t ta0 = tbase + TMEM_A_BASE + tb * NA * 64;
+        if (ATM) {
+          // the MMAs of the unit that last used this TMEM A buffer are done
+          if (ta_used[tb] && !mbar_wait(&bars->ta_free[tb], ta_ph[tb], P.limit_ns)) { fail(); break; }
+          if (ta_used[tb]) ta_ph[tb] ^= 1;
+          for (int t = 0; t < U.ntile; ++t)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              tmem_cp_128x256b(ta0 + t * 64 + 8 * k,
+                               sdesc_kmajor_sw128(a0 + t * TILE_BYTES + (k >> 2) * AHALF + (k & 3) * 32));
+          // the staging buffer is free once the copies have completed
+          mma_commit(&bars->a_empty[ab]);
+          if (++ab == ABUF) { ab = 0; aph ^= 1; }
+        }
         for (int i = 0; i < U.nT; ++i) {
           if (*abort_flag) break;
           if (!mbar_wait(&bars->b_full[s], bph, P.limit_ns)) { fail(); break; }
@@ -543,7 +570,10 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
               for (int k = 0; k < 8; ++k) {
                 const uint32_t ka = (k >> 2) * AHALF + (k & 3) * 32;
                 const uint32_t kb = (k >> 2) * BHALF + (k & 3) * 32;
-                mma_bf16(d, sdesc_kmajor_sw128(at + ka), sdesc_kmajor_sw128(b0 + kb), idesc, k > 0 ? 1u : 0u);
+                if (ATM)
+                  mma_bf16_ta(d, ta0 + t * 64 + 8 * k, sdesc_kmajor_sw128(b0 + kb), idesc, k > 0 ? 1u : 0u);
+                else
+                  mma_bf16(d, sdesc_kmajor_sw128(at + ka), sdesc_kmajor_sw128(b0 + kb), idesc, k > 0 ? 1u : 0u);
               }
             }
             // accumulator t of this tile is complete (missing tiles commit nothing new)
@@ -554,8 +584,14 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           if (++s == KST) { s = 0; bph ^= 1; }
           if (++db == DBUF) { db = 0; dph ^= 1; }
         }
-        mma_commit(&bars->a_empty[ab]);
-        if (++ab == ABUF) { ab = 0; aph ^= 1; }
+        if (ATM) {
+          mma_commit(&bars->ta_free[tb]);
+          ta_used[tb] = 1;
+          tb ^= 1;
+        } else {
+          mma_commit(&bars->a_empty[ab]);
+          if (++ab == ABUF) { ab = 0; aph ^= 1; }
+        }
       }
       // All issued MMAs must finish before TMEM is released.
       mma_commit(&bars->drain);
