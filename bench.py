@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use only this many layers (profiling cases)")
+    ap.add_argument("--proxy", choices=["keydiff", "knorm"], default="keydiff", help="stage-1 proxy")
     return ap.parse_args()
 
 
@@ -77,6 +78,7 @@ def algorithmic_work(cfg):
     b_k = L * Hkv * N * d * 2                       # one read of K
     b = {
         "keydiff": b_k + L * Hkv * N * 4,           # read K, write s
+        "knorm": b_k + L * Hkv * N * 4,             # read K, write s
         "recon_gather": L * Hq * Q * d * 2 * 2 + L * Hkv * Q * d * 2 * 2,
         "evict_topk": L * Hkv * N * 4 + L * Hkv * k * 4,
         "compact": 2 * 2 * L * Hkv * k * d * 2,     # read + write kept K and V
@@ -242,8 +244,8 @@ def run_reference(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_of(cfg):
-    return {"workload": cfg.name, "L": cfg.L, "Hkv": cfg.Hkv, "Hq": cfg.Hq, "d": cfg.d, "N": cfg.N,
+def config_of(cfg, proxy="keydiff"):
+    return {"workload": cfg.name, "proxy": proxy, "L": cfg.L, "Hkv": cfg.Hkv, "Hq": cfg.Hq, "d": cfg.d, "N": cfg.N,
             "sinks": cfg.sinks, "m": cfg.m, "rho": cfg.rho, "budget": cfg.budget, "passes": cfg.passes,
             "needle_clusters_per_layer": cfg.needles_per_layer,
             "l2": "inputs larger than L2 (K alone exceeds the 129 MB L2); no flush between steps",
@@ -280,7 +282,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step():
-        qk.kvc_compress(shape, K, V, Q, S, cfg.m, cfg.rho, cfg.passes, kl, kept, Kc, Vc, ws=ws, stream=stream)
+        qk.kvc_compress_ex(shape, args.proxy, K, V, Q, S, cfg.m, cfg.rho, cfg.passes, kl, kept, Kc, Vc, ws=ws,
+                           stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -383,7 +386,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                     Kbuf[bsel].copy_(hK, non_blocking=True)
                     ev_copied[bsel].record(copy_stream)
                 stream.wait_event(ev_copied[bsel])
-                qk.kvc_compress(shape, Kbuf[bsel], hV, hQ, S, cfg.m, cfg.rho, cfg.passes, kl, kept, Kc, Vc, ws=ws,
+                qk.kvc_compress_ex(shape, args.proxy, Kbuf[bsel], hV, hQ, S, cfg.m, cfg.rho, cfg.passes, kl, kept, Kc, Vc, ws=ws,
                                 stream=stream)
                 ev_free[bsel].record(stream)
                 hkept.copy_(kept, non_blocking=True)
@@ -429,7 +432,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(cfg),
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(cfg, args.proxy),
             "roofline": roof, "step_roofline": step_roof, "bandwidth": bw, "kernels": kernels,
             "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
         }

@@ -142,6 +142,17 @@ KVC_API size_t kvc_workspace_size(kvc_shape shape, int32_t sinks, int32_t m, dou
 KVC_API kvc_status kvc_proxy_score(kvc_shape shape, const void* K, float* p, float* s_opt, void* ws, size_t ws_bytes,
                            kvc_stream stream);
 
+/* Stage-1 proxy kinds.  KV² page, "어떻게 동작하나": KeyDiff is the default;
+ * "전제와 한계": Knorm is the close alternative.  Knorm here scores
+ * s_i = -|k_i| per (layer, KV head) (keys of smaller L2 norm rank higher),
+ * averaged over the heads like KeyDiff. */
+typedef enum { KVC_PROXY_KEYDIFF = 0, KVC_PROXY_KNORM = 1 } kvc_proxy_kind;
+
+/* kvc_proxy_score with a selectable proxy kind; same arguments, layouts and
+ * errors (KVC_ERR_INVALID for an unknown kind). */
+KVC_API kvc_status kvc_proxy_score_kind(kvc_shape shape, kvc_proxy_kind kind, const void* K, float* p, float* s_opt,
+                                        void* ws, size_t ws_bytes, kvc_stream stream);
+
 /* The pages have no counterpart to this entry point.  Same result as
  * kvc_proxy_score (p only) for callers that cannot allocate device memory
  * when they need the proxy -- runtimes that give all free HBM to their own
@@ -221,6 +232,12 @@ KVC_API kvc_status kvc_compress(kvc_shape shape, const void* K, const void* V, c
                         double rho, int32_t passes, const int32_t* k_per_layer, int32_t* kept, void* Kc, void* Vc,
                         float* p_opt, int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes,
                         kvc_stream stream);
+
+/* kvc_compress with a selectable stage-1 proxy (kvc_compress uses KeyDiff). */
+KVC_API kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K, const void* V,
+                                   const void* Qpool, int32_t sinks, int32_t m, double rho, int32_t passes,
+                                   const int32_t* k_per_layer, int32_t* kept, void* Kc, void* Vc, float* p_opt,
+                                   int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes, kvc_stream stream);
 
 /* ------------------------------------------------------------------ EpiCache
  * "[26'ICML] EpiCache", "+α: 레이어별 예산 배분": per-layer budgets from a

@@ -86,19 +86,27 @@ def keydiff_head(K: np.ndarray) -> np.ndarray:
     return s
 
 
-def proxy_scores(K: np.ndarray):
-    """Token-level proxy p_i = mean over (layer, KV head) of KeyDiff.
+def knorm_head(K: np.ndarray) -> np.ndarray:
+    """Knorm proxy of one (layer, KV head): s_i = -|k_i| (the KV² page,
+    "전제와 한계", names Knorm as the close alternative to KeyDiff; keys of
+    smaller L2 norm rank higher)."""
+    K = np.asarray(K, dtype=np.float64)
+    return -np.sqrt(np.sum(K * K, axis=1))
+
+
+def proxy_scores(K: np.ndarray, kind: str = "keydiff"):
+    """Token-level proxy p_i = mean over (layer, KV head) of the per-head
+    proxy (KeyDiff by default, or Knorm).
 
     K: float64 (or bf16 bits) [L, Hkv, N, d].  Returns (p [N], s [L, Hkv, N]).
     The pages report that the mean beat the max as the layer/head aggregate.
     """
+    head = {"keydiff": keydiff_head, "knorm": knorm_head}[kind]
+    L, H = K.shape[:2]
     if K.dtype == np.uint16:
-        L, H = K.shape[:2]
-        s = np.stack([np.stack([keydiff_head(bf16_to_f64(K[l, h])) for h in range(H)])
-                      for l in range(L)])
+        s = np.stack([np.stack([head(bf16_to_f64(K[l, h])) for h in range(H)]) for l in range(L)])
     else:
-        L, H = K.shape[:2]
-        s = np.stack([np.stack([keydiff_head(K[l, h]) for h in range(H)]) for l in range(L)])
+        s = np.stack([np.stack([head(K[l, h]) for h in range(H)]) for l in range(L)])
     p = s.reshape(L * H, -1).mean(axis=0)
     return p, s
 
@@ -278,10 +286,10 @@ def budget_count(b: float, N: int) -> int:
 # ---------------------------------------------------------------------------
 # Whole KV² pass (single or iterative)
 # ---------------------------------------------------------------------------
-def kv2_compress(K, V, Qpool, sinks, m, rho, k_per_layer, passes=1):
+def kv2_compress(K, V, Qpool, sinks, m, rho, k_per_layer, passes=1, proxy="keydiff"):
     """proxy -> passes x (select -> reconstruct -> [refine]) -> evict -> compact."""
     L, H, N, d = K.shape
-    p, _ = proxy_scores(K)
+    p, _ = proxy_scores(K, proxy)
     sel_hist = []
     for t in range(passes):
         sel, chunks = select_queries(p, N, sinks, m, rho)

@@ -78,6 +78,9 @@ _SIGS = {
     "kvc_block_prefill_step": (c_i32, [ctypes.POINTER(kvc_block_state), c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_vp,
                                        c_sz, c_vp]),
     "kvc_proxy_score_noalloc": (c_i32, [kvc_shape, c_vp, c_vp, c_vp]),
+    "kvc_proxy_score_kind": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_compress_ex": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_i32,
+                                ctypes.POINTER(c_i32), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "kvc_profile_begin": (c_i32, []),
     "kvc_profile_end": (c_i32, [ctypes.POINTER(kvc_kernel_time), c_i32, ctypes.POINTER(c_i32)]),
 }
@@ -239,6 +242,35 @@ def kvc_proxy_score(shape, K, p, s=None, ws=None, stream=None) -> None:
     _check("kvc_proxy_score", lib().kvc_proxy_score(_shape(shape), _dev(K, torch.bfloat16, "K"),
                                                     _dev(p, torch.float32, "p"), _dev(s, torch.float32, "s"),
                                                     w, wb, _stream(stream)))
+
+
+KVC_PROXY_KEYDIFF = 0
+KVC_PROXY_KNORM = 1
+_PROXY = {"keydiff": KVC_PROXY_KEYDIFF, "knorm": KVC_PROXY_KNORM}
+
+
+def _proxy_kind(kind) -> int:
+    return _PROXY[kind] if isinstance(kind, str) else int(kind)
+
+
+def kvc_proxy_score_kind(shape, kind, K, p, s=None, ws=None, stream=None) -> None:
+    """kvc_proxy_score with a proxy kind: "keydiff" (default) or "knorm"."""
+    w, wb = _ws(ws)
+    _check("kvc_proxy_score_kind", lib().kvc_proxy_score_kind(
+        _shape(shape), _proxy_kind(kind), _dev(K, torch.bfloat16, "K"), _dev(p, torch.float32, "p"),
+        _dev(s, torch.float32, "s"), w, wb, _stream(stream)))
+
+
+def kvc_compress_ex(shape, proxy, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, Kc, Vc, p=None, sel=None,
+                    score=None, ws=None, stream=None) -> None:
+    """kvc_compress with a selectable stage-1 proxy ("keydiff" or "knorm")."""
+    w, wb = _ws(ws)
+    _check("kvc_compress_ex", lib().kvc_compress_ex(
+        _shape(shape), _proxy_kind(proxy), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(V, torch.bfloat16, "V"),
+        _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"), sinks, m, float(rho), passes, _i32_array(k_per_layer),
+        _dev(kept, torch.int32, "kept"), _dev(Kc, torch.bfloat16, "Kc"), _dev(Vc, torch.bfloat16, "Vc"),
+        _dev(p, torch.float32, "p"), _dev(sel, torch.int32, "sel"), _dev(score, torch.float32, "score"), w, wb,
+        _stream(stream)))
 
 
 def kvc_proxy_score_noalloc(shape, K, p, stream=None) -> None:

@@ -418,7 +418,13 @@ size_t kvc_workspace_size(kvc_shape shape, int32_t sinks, int32_t m, double rho)
 
 kvc_status kvc_proxy_score(kvc_shape shape, const void* K, float* p, float* s_opt, void* ws, size_t ws_bytes,
                            kvc_stream stream) {
-  if (!shape_ok(shape) || !K || !p || !aligned16(K)) return KVC_ERR_INVALID;
+  return kvc_proxy_score_kind(shape, KVC_PROXY_KEYDIFF, K, p, s_opt, ws, ws_bytes, stream);
+}
+
+kvc_status kvc_proxy_score_kind(kvc_shape shape, kvc_proxy_kind kind, const void* K, float* p, float* s_opt,
+                                void* ws, size_t ws_bytes, kvc_stream stream) {
+  if (!shape_ok(shape) || !K || !p || !aligned16(K) || (kind != KVC_PROXY_KEYDIFF && kind != KVC_PROXY_KNORM))
+    return KVC_ERR_INVALID;
   float* s = s_opt;
   if (!s) {
     // per-head scratch lives in the score region of the workspace
@@ -428,7 +434,9 @@ kvc_status kvc_proxy_score(kvc_shape shape, const void* K, float* p, float* s_op
   }
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
-  return cuda_status(launch_proxy(K, shape.L * shape.Hkv, shape.N, s, p, cs(stream)));
+  const int LH = shape.L * shape.Hkv;
+  return cuda_status(kind == KVC_PROXY_KNORM ? launch_knorm(K, LH, shape.N, s, p, cs(stream))
+                                             : launch_proxy(K, LH, shape.N, s, p, cs(stream)));
 }
 
 kvc_status kvc_select_queries(int32_t N, int32_t sinks, int32_t m, double rho, const float* p, int32_t* sel,
@@ -487,7 +495,16 @@ kvc_status kvc_compress(kvc_shape shape, const void* K, const void* V, const voi
                         double rho, int32_t passes, const int32_t* k_per_layer, int32_t* kept, void* Kc, void* Vc,
                         float* p_opt, int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes,
                         kvc_stream stream) {
+  return kvc_compress_ex(shape, KVC_PROXY_KEYDIFF, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, Kc, Vc,
+                         p_opt, sel_opt, score_opt, ws, ws_bytes, stream);
+}
+
+kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K, const void* V, const void* Qpool,
+                           int32_t sinks, int32_t m, double rho, int32_t passes, const int32_t* k_per_layer,
+                           int32_t* kept, void* Kc, void* Vc, float* p_opt, int32_t* sel_opt, float* score_opt,
+                           void* ws, size_t ws_bytes, kvc_stream stream) {
   ChunkPlan plan;
+  if (proxy != KVC_PROXY_KEYDIFF && proxy != KVC_PROXY_KNORM) return KVC_ERR_INVALID;
   if (!shape_ok(shape) || !K || !Qpool || !kept || !Kc || passes < 1 || (V == nullptr) != (Vc == nullptr) ||
       !aligned16(K) || !aligned16(Qpool) || !aligned16(Kc) || (V && (!aligned16(V) || !aligned16(Vc))) ||
       !make_plan(shape.N, sinks, m, rho, &plan))
@@ -504,7 +521,9 @@ kvc_status kvc_compress(kvc_shape shape, const void* K, const void* V, const voi
   float* score = score_opt ? score_opt : w.score;
   const int LH = shape.L * shape.Hkv;
   // stage 1: proxy (per-head scratch in the score buffer)
-  if (launch_proxy(K, LH, shape.N, score, p, st) != cudaSuccess) return KVC_ERR_CUDA;
+  const cudaError_t pe = (proxy == KVC_PROXY_KNORM) ? launch_knorm(K, LH, shape.N, score, p, st)
+                                                    : launch_proxy(K, LH, shape.N, score, p, st);
+  if (pe != cudaSuccess) return KVC_ERR_CUDA;
   for (int t = 0; t < passes; ++t) {
     if (launch_select(p, shape.N, sinks, plan, rho, sel, st) != cudaSuccess) return KVC_ERR_CUDA;
     kvc_status r = run_recon(shape, plan, sinks, K, Qpool, sel, nullptr, score, nullptr, w, st);

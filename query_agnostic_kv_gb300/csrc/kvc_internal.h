@@ -71,6 +71,9 @@ bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t 
 // KeyDiff proxy: s[lh][i] for LH = L*Hkv heads of N rows, then p = mean.
 cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, cudaStream_t st);
 
+// Knorm proxy: s[lh][i] = -|k_i|, then p = mean.
+cudaError_t launch_knorm(const void* K, int LH, int N, float* s, float* p, cudaStream_t st);
+
 // p[i] = mean over LH rows of x[lh][i] (stride ld); p[i] = 0 for i < zero_below.
 cudaError_t launch_mean_heads(const float* x, int LH, int N, int64_t ld, int zero_below, float* p,
                               cudaStream_t st);

@@ -154,6 +154,36 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
   }
 }
 
+// Knorm proxy (KV² page, "전제와 한계": the close alternative to KeyDiff):
+// s_i = -|k_i| per (layer, KV head), one read of K.  Half a warp per 256-byte
+// row, eight rows in flight per half-warp.
+__global__ void __launch_bounds__(256) knorm_kernel(const uint4* __restrict__ K, int64_t rows,
+                                                    float* __restrict__ s_out) {
+  constexpr int R = 8;
+  const int l16 = threadIdx.x & 15;
+  const int64_t hw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 4);
+  for (int64_t r0 = hw; r0 < rows; r0 += stride * R) {
+    uint4 q[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      const int64_t r = r0 + u * stride;
+      q[u] = (r < rows) ? __ldg(K + r * 16 + l16) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      float f[8];
+      unpack8(q[u], f);
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ss = fmaf(f[c], f[c], ss);
+      ss = half_warp_sum(ss);
+      const int64_t r = r0 + u * stride;
+      if (l16 == 0 && r < rows) s_out[r] = -sqrtf(ss);
+    }
+  }
+}
+
 // p[i] = (1/LH) sum_h x[h][i] (fixed order), 0 below `zero_below`.
 __global__ void mean_heads_kernel(const float* __restrict__ x, int LH, int N, int64_t ld, int zero_below,
                                   float* __restrict__ p) {
@@ -179,6 +209,20 @@ cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, cudaS
     keydiff_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(static_cast<const __nv_bfloat16*>(K), N, s);
   }
   e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_mean_heads(s, LH, N, N, 0, p, st);
+}
+
+cudaError_t launch_knorm(const void* K, int LH, int N, float* s, float* p, cudaStream_t st) {
+  const int64_t rows = static_cast<int64_t>(LH) * N;
+  int64_t blocks = (rows + 16 * 8 - 1) / (16 * 8);
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  {
+    ProfScope ps("knorm", st);
+    knorm_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(K), rows, s);
+  }
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_mean_heads(s, LH, N, N, 0, p, st);
 }

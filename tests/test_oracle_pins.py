@@ -77,6 +77,20 @@ def test_keydiff_matches_cosine_library_routine():
     np.testing.assert_allclose(kv2.keydiff_head(K), ref, atol=1e-13)
 
 
+def test_knorm_closed_forms_and_aggregate():
+    """Knorm: s = -|k|; 3-4-5 keys, a zero key, scaling a key scales its
+    score, and p is the head mean."""
+    K = np.array([[3.0, 4.0], [0.0, 0.0], [6.0, 8.0], [-1.0, 0.0]])
+    np.testing.assert_allclose(kv2.knorm_head(K), [-5.0, 0.0, -10.0, -1.0], atol=0)
+    rng = np.random.default_rng(8)
+    X = rng.standard_normal((30, 16))
+    c = rng.uniform(0.1, 10.0, size=(30, 1))
+    np.testing.assert_allclose(kv2.knorm_head(X * c), kv2.knorm_head(X) * c[:, 0], rtol=1e-13)
+    np.testing.assert_allclose(-kv2.knorm_head(X), np.linalg.norm(X, axis=1), rtol=1e-14)
+    p, s = kv2.proxy_scores(np.stack([K[None], 2 * K[None]]), kind="knorm")
+    np.testing.assert_allclose(p, [-7.5, 0.0, -15.0, -1.5], atol=0)
+
+
 # ---------------------------------------------------------------------------
 # Chunk plan and query selection
 # ---------------------------------------------------------------------------

@@ -170,6 +170,47 @@ def test_compress_matches_stages_and_is_deterministic(qk):
     assert np.array_equal(res[0][0].reshape(L, H, k), stages["kept"])
 
 
+@pytest.mark.parametrize("name", ["tiny-4k", "ragged-1000"])
+def test_knorm_proxy_and_pipeline(qk, name):
+    """Knorm proxy (s = -|k|, mean over heads) against the oracle, and the
+    whole pipeline with Knorm as stage 1: selection on the GPU's p, scores
+    and eviction on the GPU's selection."""
+    cfg = CASES[name]
+    x = ks.gen_kv2(cfg)
+    L, H, Hq, N, S = cfg.L, cfg.Hkv, cfg.Hq, cfg.N, cfg.sinks
+    shape = (L, H, Hq, 128, N)
+    K, V, Q = to_dev(x.K), to_dev(x.V), to_dev(x.Q)
+    ws = torch.empty(qk.kvc_workspace_size(shape, S, cfg.m, cfg.rho), dtype=torch.uint8, device=DEV)
+    p = torch.empty(N, dtype=torch.float32, device=DEV)
+    s = torch.empty(L * H * N, dtype=torch.float32, device=DEV)
+    qk.kvc_proxy_score_kind(shape, "knorm", K, p, s, ws=ws)
+    p_ref, s_ref = kv2.proxy_scores(x.K, kind="knorm")
+    compare.assert_scores(s.cpu().numpy().reshape(L, H, N), s_ref, rtol=1e-5, what="knorm s")
+    compare.assert_scores(p.cpu().numpy(), p_ref, rtol=1e-5, what="knorm p")
+    k = qk.kvc_budget_count(cfg.budget, N, S)
+    off = qk.kvc_chunk_plan(N, S, cfg.m, cfg.rho)
+    kept = torch.empty(L * H * k, dtype=torch.int32, device=DEV)
+    Kc = torch.empty(L * H * k * 128, dtype=torch.bfloat16, device=DEV)
+    Vc = torch.empty_like(Kc)
+    p2 = torch.empty(N, dtype=torch.float32, device=DEV)
+    sel = torch.empty(off[-1], dtype=torch.int32, device=DEV)
+    score = torch.empty(L * H * N, dtype=torch.float32, device=DEV)
+    qk.kvc_compress_ex(shape, "knorm", K, V, Q, S, cfg.m, cfg.rho, 1, [k] * L, kept, Kc, Vc, p=p2, sel=sel,
+                       score=score, ws=ws)
+    assert qk.kvc_stream_status() == 0
+    assert torch.equal(p2, p)
+    sel_np = sel.cpu().numpy().astype(np.int64)
+    ref_sel, chunks = kv2.select_queries(p.cpu().numpy().astype(np.float64), N, S, cfg.m, cfg.rho)
+    assert np.array_equal(sel_np, ref_sel)
+    sc_ref, _ = kv2.recon_scores(x.K, x.Q, sel_np, chunks)
+    sc = score.cpu().numpy().reshape(L, H, N).astype(np.float64)
+    compare.assert_scores(sc[:, :, S:], sc_ref[:, :, S:], what="scores after knorm selection")
+    kept_np = kept.cpu().numpy().reshape(L, H, k)
+    for l in range(L):
+        for h in range(H):
+            compare.assert_topk_set(kept_np[l, h], sc[l, h], S, N, k - S, forced=range(S))
+
+
 def test_pinned_host_pool_and_values(qk):
     """The query pool and V may stay in pinned host memory (mapped into the
     device address space): the outputs are bit-identical to the
