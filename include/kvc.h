@@ -293,6 +293,43 @@ KVC_API kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk,
                                   const void* Qprompt, const void* Kprompt, int32_t P, void* ws, size_t ws_bytes,
                                   kvc_stream stream);
 
+/* ------------------------------------------------------------------ decode
+ * KV² page, "전제와 한계": the savings of compression reach decoding only
+ * through a compact serving backend that attends over the physically
+ * compacted cache, whose length differs per (layer, KV head).
+ *
+ * A segment is a run of rows of one KV head: rows [seg_off[s], seg_off[s] +
+ * seg_len[s]) of Kc and Vc.  Its G query heads are rows q[s][0..G-1].  For
+ * every (s, g), with z_i = scale * (q[s][g] . k_i) over the segment's rows:
+ *   out[s][g][:] = sum_i softmax(z)_i * v_i        (float32)
+ *   lse_opt[s][g] = log sum_i exp(z_i)             (natural log)
+ * A segment of length 0 gets out = 0 and lse = -inf.
+ *   Kc, Vc    device bf16 [kv_rows][128], 16-byte aligned
+ *   seg_off   device int64 [n_seg]; seg_len device int32 [n_seg]
+ *   max_len   host upper bound of every seg_len (plans the split of long
+ *             segments; must match the value given to the workspace query)
+ *   q         device bf16 [n_seg][G][128]; 1 <= G <= 8
+ *   scale     softmax scale; <= 0 selects 1/sqrt(128)
+ *   out       device f32 [n_seg][G][128]; lse_opt device f32 [n_seg][G] or NULL
+ * Segments are independent, so one call can cover every (layer, KV head) of
+ * one or many caches.  A segment with a negative or too long length, or rows
+ * outside [0, kv_rows), is skipped and reported as KVC_ERR_BOUNDS by
+ * kvc_stream_status (its output is left unwritten).  Calls sharing a
+ * workspace must be stream-ordered. */
+KVC_API size_t kvc_decode_workspace_size(int32_t n_seg, int32_t G, int32_t max_len);
+KVC_API kvc_status kvc_decode_attention(int32_t n_seg, int32_t G, const void* Kc, const void* Vc, int64_t kv_rows,
+                                        const int64_t* seg_off, const int32_t* seg_len, int32_t max_len,
+                                        const void* q, float scale, float* out, float* lse_opt, void* ws,
+                                        size_t ws_bytes, kvc_stream stream);
+
+/* Segment table of a cache laid out as kvc_compact writes it: segment
+ * s = l * Hkv + h starts at row Hkv * sum_{l' < l} k_{l'} + h * k_l and holds
+ * k_l rows.  Host-only: k_per_layer, seg_off and seg_len are host arrays of
+ * L, L*Hkv and L*Hkv entries.  The pages define no such table; it is the
+ * addressing of the compacted layout. */
+KVC_API kvc_status kvc_compact_segments(int32_t L, int32_t Hkv, const int32_t* k_per_layer, int64_t* seg_off,
+                                        int32_t* seg_len);
+
 #ifdef __cplusplus
 }
 #endif

@@ -275,3 +275,83 @@ def gen_sensitivity(cfg: EpiConfig) -> np.ndarray:
     """Seeded per-layer sensitivity vector sigma_l ~ U(0.5, 1.5) (float32)."""
     rng = np.random.Generator(np.random.PCG64(7_000_000 + cfg.seed))
     return rng.uniform(0.5, 1.5, size=cfg.L).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# decode over compacted caches
+# --------------------------------------------------------------------------
+@dataclass(frozen=True)
+class DecodeConfig:
+    """Decode attention over compacted caches: `seqs` independent sequences,
+    each with `kept` rows per KV head in the layer being decoded."""
+    name: str
+    seqs: int
+    Hkv: int
+    G: int
+    kept: int
+    needles_per_segment: int = 4
+    seed: int = 7
+
+    @property
+    def n_seg(self) -> int:
+        return self.seqs * self.Hkv
+
+
+# Llama-3.1-8B shape, 128K context compressed to a 10% budget (k = 13107 per
+# KV head), a batch of 64 sequences decoding one layer.
+DECODE_128K = DecodeConfig("llama3.1-8b-128k-10pct-decode-b64", seqs=64, Hkv=8, G=4, kept=13107)
+DECODE_TINY = DecodeConfig("decode-tiny", seqs=2, Hkv=2, G=4, kept=204)
+DECODE_CONFIGS = {c.name: c for c in (DECODE_TINY, DECODE_128K)}
+
+
+def gen_decode(cfg: DecodeConfig, device="cpu", lens=None, gap: int = 0):
+    """Seeded compacted-cache segments for decode attention, drawn with
+    torch's generator on `device` (so large caches are made in place).
+
+    Keys follow the compression workloads' recipe k = r (z + 5 * 1_C); values
+    and queries are N(0, I); each segment holds `needles_per_segment` planted
+    keys aligned to one of its queries (logit 8 at scale 1/sqrt(d)).  Rows of
+    segment s are [off_s, off_s + len_s), with `gap` unused rows before each.
+    Returns dict(K, V [rows, 128] bf16, q [n_seg, G, 128] bf16, seg_off int64,
+    seg_len int32, rows)."""
+    import torch
+
+    d = 128
+    n_seg = cfg.n_seg if lens is None else len(lens)
+    lens = [cfg.kept] * n_seg if lens is None else [int(x) for x in lens]
+    off, row = [], 0
+    for n in lens:
+        row += gap
+        off.append(row)
+        row += n
+    rows = row
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg.seed)
+    K = torch.empty(rows, d, dtype=torch.bfloat16, device=device)
+    V = torch.empty(rows, d, dtype=torch.bfloat16, device=device)
+    bias = torch.zeros(d, device=device)
+    bias[[0, 32, 64, 96]] = 5.0
+    step = 1 << 20
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        z = torch.randn(r1 - r0, d, generator=g, device=device)
+        r = torch.exp(0.3 * torch.randn(r1 - r0, 1, generator=g, device=device))
+        K[r0:r1] = (r * (z + bias)).to(torch.bfloat16)
+        V[r0:r1] = torch.randn(r1 - r0, d, generator=g, device=device).to(torch.bfloat16)
+    q = torch.randn(n_seg, cfg.G, d, generator=g, device=device).to(torch.bfloat16)
+    # needles: one per 1/NP of each segment (distinct rows), in segments of at least NP rows
+    NP = cfg.needles_per_segment
+    segs = [s for s, n in enumerate(lens) if n >= NP > 0]
+    if segs:
+        st = torch.tensor(segs, dtype=torch.int64, device=device)
+        n_t = torch.tensor([lens[s] for s in segs], dtype=torch.float64, device=device)[:, None]
+        o_t = torch.tensor([off[s] for s in segs], dtype=torch.int64, device=device)[:, None]
+        u = torch.rand(len(segs), NP, generator=g, device=device, dtype=torch.float64)
+        t = torch.arange(NP, device=device, dtype=torch.float64)[None, :]
+        pos = torch.floor((t + u) * n_t / NP).to(torch.int64)
+        qq = q.float()[st[:, None], (torch.arange(NP, device=device) % cfg.G)[None, :]]
+        kn = 8.0 * math.sqrt(d) * qq / (qq * qq).sum(-1, keepdim=True)
+        K[(o_t + pos).reshape(-1)] = kn.reshape(-1, d).to(torch.bfloat16)
+    return dict(K=K, V=V, q=q, rows=rows,
+                seg_off=torch.tensor(off, dtype=torch.int64, device=device),
+                seg_len=torch.tensor(lens, dtype=torch.int32, device=device))

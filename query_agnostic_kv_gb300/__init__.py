@@ -81,6 +81,11 @@ _SIGS = {
     "kvc_proxy_score_kind": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "kvc_compress_ex": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_i32,
                                 ctypes.POINTER(c_i32), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_decode_workspace_size": (c_sz, [c_i32, c_i32, c_i32]),
+    "kvc_decode_attention": (c_i32, [c_i32, c_i32, c_vp, c_vp, c_i64, c_vp, c_vp, c_i32, c_vp, ctypes.c_float, c_vp,
+                                     c_vp, c_vp, c_sz, c_vp]),
+    "kvc_compact_segments": (c_i32, [c_i32, c_i32, ctypes.POINTER(c_i32), ctypes.POINTER(c_i64),
+                                     ctypes.POINTER(c_i32)]),
     "kvc_profile_begin": (c_i32, []),
     "kvc_profile_end": (c_i32, [ctypes.POINTER(kvc_kernel_time), c_i32, ctypes.POINTER(c_i32)]),
 }
@@ -323,6 +328,37 @@ def kvc_compress(shape, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, K
         _dev(kept, torch.int32, "kept"), _dev(Kc, torch.bfloat16, "Kc"), _dev(Vc, torch.bfloat16, "Vc"),
         _dev(p, torch.float32, "p"), _dev(sel, torch.int32, "sel"), _dev(score, torch.float32, "score"), w, wb,
         _stream(stream)))
+
+
+# ---------------------------------------------------------------- decode attention
+def kvc_decode_workspace_size(n_seg: int, G: int, max_len: int) -> int:
+    return int(lib().kvc_decode_workspace_size(n_seg, G, max_len))
+
+
+def kvc_decode_attention(Kc, Vc, seg_off, seg_len, max_len, q, out, lse=None, scale=0.0, ws=None,
+                         stream=None) -> None:
+    """Decode attention of q [n_seg, G, 128] over the segments (seg_off,
+    seg_len) of Kc/Vc [rows, 128]; writes out [n_seg, G, 128] (float32) and
+    optionally lse [n_seg, G]."""
+    if q.dim() != 3:
+        raise ValueError("q must be [n_seg, G, 128]")
+    n_seg, G = int(q.shape[0]), int(q.shape[1])
+    if Kc.shape != Vc.shape or Kc.dim() != 2:
+        raise ValueError("Kc and Vc must both be [rows, 128]")
+    w, wb = _ws(ws)
+    _check("kvc_decode_attention", lib().kvc_decode_attention(
+        n_seg, G, _dev(Kc, torch.bfloat16, "Kc"), _dev(Vc, torch.bfloat16, "Vc"), int(Kc.shape[0]),
+        _dev(seg_off, torch.int64, "seg_off"), _dev(seg_len, torch.int32, "seg_len"), int(max_len),
+        _dev(q, torch.bfloat16, "q"), float(scale), _dev(out, torch.float32, "out"), _dev(lse, torch.float32, "lse"),
+        w, wb, _stream(stream)))
+
+
+def kvc_compact_segments(L: int, Hkv: int, k_per_layer) -> tuple[list[int], list[int]]:
+    """(row offsets, lengths) of the (layer, KV head) segments of a compacted cache."""
+    off = (c_i64 * (L * Hkv))()
+    ln = (c_i32 * (L * Hkv))()
+    _check("kvc_compact_segments", lib().kvc_compact_segments(L, Hkv, _i32_array(k_per_layer), off, ln))
+    return list(off), list(ln)
 
 
 # ---------------------------------------------------------------- EpiCache block prefill

@@ -766,3 +766,93 @@ kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk, const v
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- decode attention
+namespace {
+
+struct DecodeWorkspace {
+  float* part_o = nullptr;
+  float* part_ml = nullptr;
+  int32_t* ticket = nullptr;
+  size_t bytes = 0;
+  bool ok = false;
+};
+
+DecodeWorkspace carve_decode(int32_t n_seg, int32_t G, const DecodePlan& pl, void* base, size_t cap) {
+  DecodeWorkspace w;
+  Carver c(base, base ? cap : 0);
+  const int64_t parts = pl.n_split > 1 ? int64_t(n_seg) * pl.n_split * G : 0;
+  w.part_o = c.take<float>(parts * kHeadDim);
+  w.part_ml = c.take<float>(parts * 2);
+  w.ticket = c.take<int32_t>(pl.n_split > 1 ? n_seg : 0);
+  w.bytes = ((c.used + 255) & ~size_t(255)) + 256;
+  w.ok = c.ok;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvc_decode_workspace_size(int32_t n_seg, int32_t G, int32_t max_len) {
+  if (n_seg < 0 || G < 1 || G > 8 || max_len < 0) return 0;
+  return carve_decode(n_seg, G, make_decode_plan(n_seg, max_len), nullptr, 0).bytes;
+}
+
+kvc_status kvc_decode_attention(int32_t n_seg, int32_t G, const void* Kc, const void* Vc, int64_t kv_rows,
+                                const int64_t* seg_off, const int32_t* seg_len, int32_t max_len, const void* q,
+                                float scale, float* out, float* lse_opt, void* ws, size_t ws_bytes,
+                                kvc_stream stream) {
+  if (n_seg < 0 || G < 1 || G > 8 || max_len < 0 || kv_rows < 0) return KVC_ERR_INVALID;
+  if (n_seg == 0) return KVC_OK;
+  if (!Kc || !Vc || !seg_off || !seg_len || !q || !out || !aligned16(Kc) || !aligned16(Vc) || !aligned16(q) ||
+      (reinterpret_cast<uintptr_t>(out) & 3u) != 0 || (lse_opt && (reinterpret_cast<uintptr_t>(lse_opt) & 3u)))
+    return KVC_ERR_INVALID;
+  if (int64_t(n_seg) * G * kHeadDim >= (int64_t(1) << 31)) return KVC_ERR_INVALID;
+  const DecodePlan pl = make_decode_plan(n_seg, max_len);
+  if (int64_t(n_seg) * pl.n_split >= (int64_t(1) << 31)) return KVC_ERR_INVALID;
+  DecodeWorkspace w = carve_decode(n_seg, G, pl, ws, ws_bytes);
+  if (check_ws(ws, ws_bytes, w.bytes) != KVC_OK || !w.ok) return KVC_ERR_WORKSPACE;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  DecodeParams p{};
+  p.K = static_cast<const uint16_t*>(Kc);
+  p.V = static_cast<const uint16_t*>(Vc);
+  p.seg_off = seg_off;
+  p.seg_len = seg_len;
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = out;
+  p.lse = lse_opt;
+  p.part_o = w.part_o;
+  p.part_ml = w.part_ml;
+  p.ticket = w.ticket;
+  p.kv_rows = kv_rows;
+  p.n_seg = n_seg;
+  p.G = G;
+  p.max_len = max_len;
+  p.CH = pl.CH;
+  p.n_split = pl.n_split;
+  const double sc = scale > 0.f ? double(scale) : 1.0 / std::sqrt(double(kHeadDim));
+  p.sc2 = static_cast<float>(sc * 1.4426950408889634);
+  p.status = status_word();
+  p.limit_ns = wait_limit_ns();
+  if (!p.status) return KVC_ERR_CUDA;
+  return cuda_status(launch_decode(p, cs(stream)));
+}
+
+kvc_status kvc_compact_segments(int32_t L, int32_t Hkv, const int32_t* k_per_layer, int64_t* seg_off,
+                                int32_t* seg_len) {
+  if (L < 1 || Hkv < 1 || !k_per_layer || !seg_off || !seg_len) return KVC_ERR_INVALID;
+  int64_t row = 0;
+  for (int32_t l = 0; l < L; ++l) {
+    if (k_per_layer[l] < 0) return KVC_ERR_INVALID;
+    for (int32_t h = 0; h < Hkv; ++h) {
+      seg_off[int64_t(l) * Hkv + h] = row;
+      seg_len[int64_t(l) * Hkv + h] = k_per_layer[l];
+      row += k_per_layer[l];
+    }
+  }
+  return KVC_OK;
+}
+
+}  // extern "C"

@@ -164,4 +164,29 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
 // Device-side wait that expires on purpose (status-path test).
 cudaError_t launch_expire_wait(uint64_t limit_ns, cudaStream_t st);
 
+// Decode attention over ragged segments of a compacted cache.
+struct DecodePlan {
+  int32_t CH = 0;        // keys per split (multiple of the tile)
+  int32_t n_split = 0;   // splits per segment (covers max_len)
+};
+DecodePlan make_decode_plan(int32_t n_seg, int32_t max_len);
+struct DecodeParams {
+  const uint16_t* K;
+  const uint16_t* V;
+  const int64_t* seg_off;
+  const int32_t* seg_len;
+  const uint16_t* q;      // [n_seg][G][128]
+  float* out;             // [n_seg][G][128]
+  float* lse;             // [n_seg][G] or null
+  float* part_o;          // [n_seg][n_split][G][128]
+  float* part_ml;         // [n_seg][n_split][G][2]
+  int32_t* ticket;        // [n_seg], zero on entry
+  int64_t kv_rows;
+  int32_t n_seg, G, max_len, CH, n_split;
+  float sc2;              // softmax scale * log2(e)
+  int* status;
+  uint64_t limit_ns;
+};
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+
 }  // namespace kvc

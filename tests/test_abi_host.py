@@ -92,6 +92,26 @@ def test_invalid_arguments_rejected_on_host(qk):
     assert qk.kvc_workspace_size((1, 1, 4, 128, 4096), 4, 1024, 0.1) > 0
 
 
+def test_compact_segments_match_oracle(qk):
+    from oracle import decode
+    kl = [7, 0, 12, 3]
+    off, ln = qk.kvc_compact_segments(4, 3, kl)
+    ro, rl = decode.compact_segments(4, 3, kl)
+    assert off == ro.tolist() and ln == rl.tolist()
+    with pytest.raises(qk.KVCError):
+        qk.kvc_compact_segments(2, 2, [3, -1])
+
+
+def test_decode_workspace_query(qk):
+    assert qk.kvc_decode_workspace_size(8, 0, 100) == 0          # G < 1
+    assert qk.kvc_decode_workspace_size(8, 9, 100) == 0          # G > 8
+    small = qk.kvc_decode_workspace_size(8, 4, 300)
+    big = qk.kvc_decode_workspace_size(512, 4, 13107)
+    assert 0 < small < big
+    # split partials: n_seg * n_split * G * (128 + 2) floats at most ~ 32 items per SM
+    assert big < 512 * 64 * 4 * 130 * 4 + 4096
+
+
 def test_status_strings(qk):
     for code in range(7):
         assert qk.kvc_status_string(code).startswith("KVC_")
