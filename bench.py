@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use only this many layers (profiling cases)")
     ap.add_argument("--proxy", choices=["keydiff", "knorm"], default="keydiff", help="stage-1 proxy")
+    ap.add_argument("--op", choices=["compress", "decode"], default="compress",
+                    help="compress: the KV² compression step; decode: attention over the compacted cache")
+    ap.add_argument("--decode-config", default=ks.DECODE_128K.name, choices=list(ks.DECODE_CONFIGS))
     return ap.parse_args()
 
 
@@ -439,6 +442,183 @@ def run_ours(args, cfg, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- decode attention leg
+DECODE_METRIC = "decode attention over compacted KV caches: algorithmic HBM GB/s"
+
+
+def decode_bytes(cfg):
+    """Algorithmic bytes of one decode launch: every kept K and V row once,
+    the queries, the outputs and their lse."""
+    rows = cfg.n_seg * cfg.kept
+    return rows * 128 * 2 * 2 + cfg.n_seg * cfg.G * (128 * 2 + 128 * 4 + 4)
+
+
+def decode_config_of(cfg):
+    return {"workload": cfg.name, "seqs": cfg.seqs, "Hkv": cfg.Hkv, "G": cfg.G, "kept_rows_per_head": cfg.kept,
+            "d": 128, "layers_per_step": 1,
+            "l2": "inputs larger than L2 (3.4 GB of K and V); no flush between steps",
+            "parallelism": "independent batch per GPU"}
+
+
+def time_decode_oracle(cfg, x, budget_s=15.0):
+    """Oracle on whole sampled segments (host copies), scaled to a full launch."""
+    from oracle import decode
+    K = x["K"]
+    rng = np.random.default_rng(1)
+    t_used, done = 0.0, 0
+    while done == 0 or (t_used < budget_s and done < cfg.n_seg):
+        s = int(rng.integers(cfg.n_seg))
+        o, n = int(x["seg_off"][s]), int(x["seg_len"][s])
+        Ks = K[o:o + n].double().cpu().numpy()
+        Vs = x["V"][o:o + n].double().cpu().numpy()
+        q = x["q"][s:s + 1].double().cpu().numpy()
+        a = time.perf_counter()
+        decode.decode_attention(Ks, Vs, [0], [n], q)
+        t_used += time.perf_counter() - a
+        done += 1
+    per_launch = t_used / done * cfg.n_seg
+    return per_launch, f"{done} whole segments of {cfg.kept} rows (G={cfg.G}) timed, scaled x{cfg.n_seg / done:.1f}"
+
+
+def run_decode(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import query_agnostic_kv_gb300 as qk
+    from query_agnostic_kv_gb300 import _build
+
+    cfg = ks.DECODE_CONFIGS[args.decode_config]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        x = ks.gen_decode(ks.DecodeConfig(**{**cfg.__dict__, "seed": cfg.seed}), "cpu")
+        for _ in range(args.warmup):
+            time_decode_oracle(cfg, x, budget_s=0.0)
+        samples, desc = [], ""
+        for _ in range(args.steps):
+            t, desc = time_decode_oracle(cfg, x, budget_s=2.0)
+            samples.append(t)
+        t = statistics.median(samples)
+        v = decode_bytes(cfg) / t / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": DECODE_METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": decode_config_of(cfg),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _build.build_library()
+    qk.kvc_device_check()
+    x = ks.gen_decode(ks.DecodeConfig(**{**cfg.__dict__, "seed": cfg.seed + rank}), dev)
+    n_seg, G = cfg.n_seg, cfg.G
+    ws = torch.empty(qk.kvc_decode_workspace_size(n_seg, G, cfg.kept), dtype=torch.uint8, device=dev)
+    out = torch.empty(n_seg, G, 128, dtype=torch.float32, device=dev)
+    lse = torch.empty(n_seg, G, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(q=None):
+        qk.kvc_decode_attention(x["K"], x["V"], x["seg_off"], x["seg_len"], cfg.kept, x["q"] if q is None else q,
+                                out, lse, ws=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = qk.kvc_stream_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {qk.kvc_status_string(st)}")
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.6)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    qk.kvc_profile_begin()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = qk.kvc_profile_end()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    st = qk.kvc_stream_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {qk.kvc_status_string(st)}")
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    B = decode_bytes(cfg)
+    value = world * B * args.steps / (ms / 1e3) / 1e9
+    peaks, peak_src = load_peaks()
+    hbm = peaks.get("hbm_gbs")
+    n_l, tot = prof["decode_attn"]
+    ach = B / (tot / n_l / 1e3) / 1e9
+    roof = {"kernel": "decode_attn (bulk-copy ring, CUDA-core f32x2)", "bound": "hbm", "achieved": ach,
+            "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+            "peak_source": f"hbm_gbs of {peak_src} peaks", "algorithmic_bytes_per_launch": B}
+    kernels = {n: {"launches": v[0], "avg_ms": v[1] / v[0]} for n, v in prof.items()}
+
+    # end to end: this step's queries from pinned host memory in, outputs and lse back out
+    e2e = None
+    if args.e2e_steps > 0:
+        hq = x["q"].cpu().pin_memory()
+        dq = torch.empty_like(x["q"])
+        hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            step(dq)
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * B * args.e2e_steps / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hq.numel() * 2, "d2h_bytes_per_step": (hout.numel() + hlse.numel()) * 4,
+               "ms_per_step": e_ms / args.e2e_steps,
+               "how": "the compacted cache is resident (serving state); each step copies its queries from pinned "
+                      "host memory and its outputs and lse back to pinned host memory"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xh = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in x.items()}
+        t, desc = time_decode_oracle(cfg, xh)
+        cpu = {"value": B / t / 1e9, "unit": "GB/s", "cores": cores(), "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps({
+            "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": decode_config_of(cfg),
+            "roofline": roof, "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()),
+            "clocks": clocks, "e2e": e2e,
+            "cpu_baseline": cpu}), flush=True)
+
+
 def main():
     args = parse()
     cfg = ks.KV2_CONFIGS[args.config]
@@ -447,6 +627,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.op == "decode" and args.impl == "reference":
+        run_decode(args, rank, world, local_rank)
+        return
     if args.impl == "reference":
         run_reference(args, cfg, rank, world)
         return
@@ -456,7 +639,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run_ours(args, cfg, rank, world, local_rank)
+        if args.op == "decode":
+            run_decode(args, rank, world, local_rank)
+        else:
+            run_ours(args, cfg, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -300,8 +300,9 @@ class DecodeConfig:
 # Llama-3.1-8B shape, 128K context compressed to a 10% budget (k = 13107 per
 # KV head), a batch of 64 sequences decoding one layer.
 DECODE_128K = DecodeConfig("llama3.1-8b-128k-10pct-decode-b64", seqs=64, Hkv=8, G=4, kept=13107)
+DECODE_128K_B16 = DecodeConfig("llama3.1-8b-128k-10pct-decode-b16", seqs=16, Hkv=8, G=4, kept=13107)
 DECODE_TINY = DecodeConfig("decode-tiny", seqs=2, Hkv=2, G=4, kept=204)
-DECODE_CONFIGS = {c.name: c for c in (DECODE_TINY, DECODE_128K)}
+DECODE_CONFIGS = {c.name: c for c in (DECODE_TINY, DECODE_128K_B16, DECODE_128K)}
 
 
 def gen_decode(cfg: DecodeConfig, device="cpu", lens=None, gap: int = 0):

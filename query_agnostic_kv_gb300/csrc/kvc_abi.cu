@@ -773,7 +773,7 @@ namespace {
 struct DecodeWorkspace {
   float* part_o = nullptr;
   float* part_ml = nullptr;
-  int32_t* ticket = nullptr;
+  int32_t* counter = nullptr;
   size_t bytes = 0;
   bool ok = false;
 };
@@ -784,7 +784,7 @@ DecodeWorkspace carve_decode(int32_t n_seg, int32_t G, const DecodePlan& pl, voi
   const int64_t parts = pl.n_split > 1 ? int64_t(n_seg) * pl.n_split * G : 0;
   w.part_o = c.take<float>(parts * kHeadDim);
   w.part_ml = c.take<float>(parts * 2);
-  w.ticket = c.take<int32_t>(pl.n_split > 1 ? n_seg : 0);
+  w.counter = c.take<int32_t>(64);
   w.bytes = ((c.used + 255) & ~size_t(255)) + 256;
   w.ok = c.ok;
   return w;
@@ -825,7 +825,7 @@ kvc_status kvc_decode_attention(int32_t n_seg, int32_t G, const void* Kc, const 
   p.lse = lse_opt;
   p.part_o = w.part_o;
   p.part_ml = w.part_ml;
-  p.ticket = w.ticket;
+  p.counter = w.counter;
   p.kv_rows = kv_rows;
   p.n_seg = n_seg;
   p.G = G;

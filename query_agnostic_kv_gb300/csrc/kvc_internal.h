@@ -178,9 +178,9 @@ struct DecodeParams {
   const uint16_t* q;      // [n_seg][G][128]
   float* out;             // [n_seg][G][128]
   float* lse;             // [n_seg][G] or null
-  float* part_o;          // [n_seg][n_split][G][128]
-  float* part_ml;         // [n_seg][n_split][G][2]
-  int32_t* ticket;        // [n_seg], zero on entry
+  float* part_o;          // [n_seg][n_split][G][128] (splits of multi-split segments)
+  float* part_ml;         // [n_seg][n_split][G][2]: base-2 max, sum
+  int32_t* counter;       // work-item counter, zero on entry
   int64_t kv_rows;
   int32_t n_seg, G, max_len, CH, n_split;
   float sc2;              // softmax scale * log2(e)
