@@ -796,7 +796,7 @@ extern "C" {
 
 size_t kvc_decode_workspace_size(int32_t n_seg, int32_t G, int32_t max_len) {
   if (n_seg < 0 || G < 1 || G > 8 || max_len < 0) return 0;
-  return carve_decode(n_seg, G, make_decode_plan(n_seg, max_len), nullptr, 0).bytes;
+  return carve_decode(n_seg, G, make_decode_plan(n_seg, G, max_len), nullptr, 0).bytes;
 }
 
 kvc_status kvc_decode_attention(int32_t n_seg, int32_t G, const void* Kc, const void* Vc, int64_t kv_rows,
@@ -809,7 +809,7 @@ kvc_status kvc_decode_attention(int32_t n_seg, int32_t G, const void* Kc, const 
       (reinterpret_cast<uintptr_t>(out) & 3u) != 0 || (lse_opt && (reinterpret_cast<uintptr_t>(lse_opt) & 3u)))
     return KVC_ERR_INVALID;
   if (int64_t(n_seg) * G * kHeadDim >= (int64_t(1) << 31)) return KVC_ERR_INVALID;
-  const DecodePlan pl = make_decode_plan(n_seg, max_len);
+  const DecodePlan pl = make_decode_plan(n_seg, G, max_len);
   if (int64_t(n_seg) * pl.n_split >= (int64_t(1) << 31)) return KVC_ERR_INVALID;
   DecodeWorkspace w = carve_decode(n_seg, G, pl, ws, ws_bytes);
   if (check_ws(ws, ws_bytes, w.bytes) != KVC_OK || !w.ok) return KVC_ERR_WORKSPACE;

@@ -36,26 +36,33 @@ namespace {
 
 constexpr int D = kHeadDim;
 constexpr int ROW_BYTES = D * 2;
-constexpr int STAGES = 4;
 constexpr int LPK = 16;                      // lanes per key
 constexpr int LOG2_LPK = 4;
 constexpr int KPW = 32 / LPK;                // keys per warp per batch
 constexpr float REBASE = 16.f;               // log2 units
 constexpr int kTargetItems = 4864;           // work items aimed for (32 per SM)
 constexpr int kMinSplit = 512;               // keys
-constexpr int kSplitQuantum = 192;           // split sizes are multiples of every tile size
 constexpr int HDR_BYTES = 128;
+
+#ifndef KVC_DEC_NW
+#define KVC_DEC_NW 15
+#endif
+#ifndef KVC_DEC_STAGES
+#define KVC_DEC_STAGES 3
+#endif
 
 template <int GP>
 struct DCfg {
-  static constexpr int NW = GP <= 4 ? 12 : 8;        // consumer warps
-  static constexpr int NB = GP <= 4 ? 4 : 2;         // batches per warp per tile
-  static constexpr int TK = KPW * NW * NB;           // keys per stage (96 or 32)
+  static constexpr int NW = GP <= 4 ? KVC_DEC_NW : 8;        // consumer warps
+  static constexpr int NB = GP <= 4 ? 4 : 2;                 // batches per warp per tile
+  static constexpr int STAGES = GP <= 4 ? KVC_DEC_STAGES : 6;
+  static constexpr int TK = KPW * NW * NB;                   // keys per stage
   static constexpr int TILE_BYTES = TK * ROW_BYTES;  // one of K or V
   static constexpr int QBYTES = GP * ROW_BYTES;      // the item's queries (first tile)
   static constexpr int STAGE_BYTES = HDR_BYTES + QBYTES + 2 * TILE_BYTES;
   static constexpr int THREADS = (NW + 1) * 32;
-  static constexpr int COMB_FLOATS = NW * GP * (D + 2);
+  static constexpr int ML_FLOATS = (2 * NW * GP + 3) / 4 * 4;   // sM, sL padded to whole float4s
+  static constexpr int COMB_FLOATS = ML_FLOATS + NW * GP * D;
   static constexpr size_t SMEM = 128 + size_t(STAGES) * STAGE_BYTES + size_t(COMB_FLOATS) * 4 + 256;
 };
 
@@ -69,9 +76,10 @@ struct StageHdr {
   int32_t pad;
 };
 
+constexpr int MAX_STAGES = 8;
 struct DBars {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t comb_full;   // every consumer warp has written its partial
   uint64_t comb_free;   // every consumer warp has read the merged partials
   int abort_flag;
@@ -102,23 +110,27 @@ __device__ __forceinline__ float sum2(uint64_t a) {
   return x + y;
 }
 
-// Reduce-scatter GP partial sums over the LPK lanes of a key: afterwards lane
-// holds the full sum of value (lane % LPK) / (LPK / GP).
+// Slot permutation of a lane: slot i of lane `lane` holds query i ^ qmask.
+// With it every lane keeps the low half of its slots and sends the high half
+// at each reduce-scatter step, so the exchange needs no selects.
 template <int GP>
-__device__ __forceinline__ float reduce_scatter(float (&v)[GP], int lane) {
+__device__ __forceinline__ int slot_mask(int lane) {
+  return (lane & (LPK - 1)) / (LPK / GP);
+}
+
+// Reduce-scatter GP partial sums over the LPK lanes of a key (slots permuted
+// by slot_mask): afterwards the lane holds the full sum of query
+// (lane % LPK) / (LPK / GP).
+template <int GP>
+__device__ __forceinline__ float reduce_scatter(float (&v)[GP]) {
 #pragma unroll
   for (int st = 0; st < LOG2_LPK; ++st) {
     const int o = (LPK / 2) >> st;
     const int n = GP >> st;
     if (n > 1) {
       const int h = n / 2;
-      const bool up = (lane & o) != 0;
 #pragma unroll
-      for (int i = 0; i < h; ++i) {
-        const float send = up ? v[i] : v[i + h];
-        const float keep = up ? v[i + h] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-      }
+      for (int i = 0; i < h; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + h], o);
     } else {
       v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
     }
@@ -142,13 +154,19 @@ __global__ void __launch_bounds__(DCfg<GP>::THREADS, 1) decode_kernel(const Deco
   constexpr int TK = C::TK;
   constexpr int TILE_BYTES = C::TILE_BYTES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
-  static_assert(kSplitQuantum % TK == 0, "split quantum must be a multiple of the tile");
+  constexpr int STAGES = C::STAGES;
+  static_assert(STAGES <= MAX_STAGES, "too many stages");
+  static_assert(C::SMEM <= 232448, "shared memory per CTA exceeds 227 KB");
+  static_assert(STAGE_BYTES % 16 == 0, "stages must stay 16-byte aligned");
+  static_assert((HDR_BYTES + C::QBYTES) % 16 == 0 && TILE_BYTES % 16 == 0, "bulk-copy targets must be 16-byte aligned");
+  static_assert((size_t(STAGES) * STAGE_BYTES) % 16 == 0, "combine area must be 16-byte aligned");
+  static_assert(C::ML_FLOATS % 4 == 0 && (C::COMB_FLOATS * 4) % 8 == 0, "float4 partials and mbarriers alignment");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   float* sComb = reinterpret_cast<float*>(sbase + size_t(STAGES) * STAGE_BYTES);
   float* sM = sComb;                          // [NW][GP]
   float* sL = sM + NW * GP;                   // [NW][GP]
-  float* sAcc = sL + NW * GP;                 // [NW][GP][D]
+  float* sAcc = sComb + C::ML_FLOATS;         // [NW][GP][D], 16-byte aligned
   DBars* bars = reinterpret_cast<DBars*>(sComb + C::COMB_FLOATS);
 
   const int tid = threadIdx.x;
@@ -258,6 +276,7 @@ __global__ void __launch_bounds__(DCfg<GP>::THREADS, 1) decode_kernel(const Deco
   constexpr int DUP = LPK / GP;              // lanes holding the same (key, query) logit
   const int lq = j / DUP;                    // query index of this lane's logit
   const bool rep = (j % DUP) == 0;
+  const int qmask = slot_mask<GP>(lane);
   int s = 0;
   uint32_t ph = 0, cph = 0;
   uint64_t qv[GP][4];
@@ -279,11 +298,12 @@ __global__ void __launch_bounds__(DCfg<GP>::THREADS, 1) decode_kernel(const Deco
     const StageHdr h = *reinterpret_cast<const StageHdr*>(st);
     if (h.end) break;
     if (h.t == 0) {
-      // new item: its queries, pre-scaled to base-2 logits
+      // new item: its queries, pre-scaled to base-2 logits, in this lane's slot order
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
+        const int qg = g ^ qmask;
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (g < P.G) w = lds128(st + HDR_BYTES + g * ROW_BYTES + j * 16);
+        if (qg < P.G) w = lds128(st + HDR_BYTES + qg * ROW_BYTES + j * 16);
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -319,7 +339,7 @@ __global__ void __launch_bounds__(DCfg<GP>::THREADS, 1) decode_kernel(const Deco
           a = fma2(k3, qv[g][3], a);
           part[g] = sum2(a);
         }
-        const float z = reduce_scatter<GP>(part, lane);
+        const float z = reduce_scatter<GP>(part);
         sc[b] = valid ? z : -INFINITY;
       }
       // ---- online softmax (per warp, per query; lazily rebased)
@@ -506,10 +526,15 @@ cudaError_t launch_gp(const DecodeParams& p, int grid, cudaStream_t st) {
 
 namespace kvc {
 
-DecodePlan make_decode_plan(int32_t n_seg, int32_t max_len) {
+int32_t decode_tile_keys(int32_t G) {
+  return G <= 1 ? DCfg<1>::TK : G <= 2 ? DCfg<2>::TK : G <= 4 ? DCfg<4>::TK : DCfg<8>::TK;
+}
+
+DecodePlan make_decode_plan(int32_t n_seg, int32_t G, int32_t max_len) {
   DecodePlan pl;
+  const int32_t q = decode_tile_keys(G);   // splits are whole tiles
   if (n_seg < 1 || max_len < 1) {
-    pl.CH = kSplitQuantum;
+    pl.CH = q;
     pl.n_split = 1;
     return pl;
   }
@@ -518,7 +543,7 @@ DecodePlan make_decode_plan(int32_t n_seg, int32_t max_len) {
   want = want < cap ? want : cap;
   if (want < 1) want = 1;
   int64_t ch = (int64_t(max_len) + want - 1) / want;
-  ch = (ch + kSplitQuantum - 1) / kSplitQuantum * kSplitQuantum;
+  ch = (ch + q - 1) / q * q;
   pl.CH = static_cast<int32_t>(ch);
   pl.n_split = static_cast<int32_t>((int64_t(max_len) + ch - 1) / ch);
   return pl;

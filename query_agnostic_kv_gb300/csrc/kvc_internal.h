@@ -166,10 +166,10 @@ cudaError_t launch_expire_wait(uint64_t limit_ns, cudaStream_t st);
 
 // Decode attention over ragged segments of a compacted cache.
 struct DecodePlan {
-  int32_t CH = 0;        // keys per split (multiple of the tile)
+  int32_t CH = 0;        // keys per split (whole tiles)
   int32_t n_split = 0;   // splits per segment (covers max_len)
 };
-DecodePlan make_decode_plan(int32_t n_seg, int32_t max_len);
+DecodePlan make_decode_plan(int32_t n_seg, int32_t G, int32_t max_len);
 struct DecodeParams {
   const uint16_t* K;
   const uint16_t* V;
