@@ -453,6 +453,13 @@ def decode_bytes(cfg):
     return rows * 128 * 2 * 2 + cfg.n_seg * cfg.G * (128 * 2 + 128 * 4 + 4)
 
 
+# DRAM bytes per launch per sequence of decode_kernel as ncu counted them on the
+# 16-sequence case (dram__bytes_read + dram__bytes_write = 867.78 MB / 16); the
+# kernel's traffic grows in proportion to the rows.  Reset to None whenever the
+# kernel changes until it is captured again.
+DECODE_TRAFFIC_PER_SEQ = 867.78e6 / 16
+
+
 def decode_config_of(cfg):
     return {"workload": cfg.name, "seqs": cfg.seqs, "Hkv": cfg.Hkv, "G": cfg.G, "kept_rows_per_head": cfg.kept,
             "d": 128, "layers_per_step": 1,
@@ -566,7 +573,9 @@ def run_decode(args, rank, world, local_rank):
     n_l, tot = prof["decode_attn"]
     ach = B / (tot / n_l / 1e3) / 1e9
     roof = {"kernel": "decode_attn (bulk-copy ring, CUDA-core f32x2)", "bound": "hbm", "achieved": ach,
-            "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+            "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+            "traffic": None if DECODE_TRAFFIC_PER_SEQ is None else DECODE_TRAFFIC_PER_SEQ * cfg.seqs,
+            "traffic_source": "ncu dram bytes of the 16-sequence case, scaled by sequences",
             "peak_source": f"hbm_gbs of {peak_src} peaks", "algorithmic_bytes_per_launch": B}
     kernels = {n: {"launches": v[0], "avg_ms": v[1] / v[0]} for n, v in prof.items()}
 
