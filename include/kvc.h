@@ -330,6 +330,44 @@ KVC_API kvc_status kvc_decode_attention(int32_t n_seg, int32_t G, const void* Kc
 KVC_API kvc_status kvc_compact_segments(int32_t L, int32_t Hkv, const int32_t* k_per_layer, int64_t* seg_off,
                                         int32_t* seg_len);
 
+/* ------------------------------------------------------------------ EpiCache per turn
+ * "[26'ICML] EpiCache", "방법: 3단계" step ③ and Fig. 3: each turn the
+ * question's embedding is matched to the closest episode and that episode's
+ * compressed cache is brought in (a completely new topic gets a new cache);
+ * idle episode caches wait in host memory.
+ *
+ * Closest episode of each question: episode[b] = argmin_e |q_b - c_e|^2
+ * (squared Euclidean, fp32 accumulation; equal distances go to the lower e);
+ * with tau > 0, a question whose closest centroid is farther than tau gets -1.
+ *   queries    device f32 [B][De]; centroids device f32 [E][De]; De a
+ *              multiple of 4, both 16-byte aligned
+ *   episode    device int32 [B] (output)
+ *   dist2_opt  device f32 [B][E] squared distances, or NULL */
+KVC_API kvc_status kvc_episode_match(int32_t B, int32_t E, int32_t De, const float* queries, const float* centroids,
+                                     float tau, int32_t* episode, float* dist2_opt, kvc_stream stream);
+
+/* Rows of an episode's packed cache: Hkv * sum_l len[l] (host-only; -1 for
+ * an invalid state). */
+KVC_API int64_t kvc_episode_rows(const kvc_block_state* st);
+
+/* Packs the kept rows of a block-prefill state into one contiguous image in
+ * the compacted layout (segment (l, h) holds len[l] rows; kvc_compact_segments
+ * with k_l = len[l] addresses it), so one copy moves the whole episode and
+ * kvc_decode_attention reads it in place.
+ *   Kp, Vp    device bf16 [kvc_episode_rows][128] (output)
+ *   pos_opt   device int32 [kvc_episode_rows] global positions, or NULL */
+KVC_API kvc_status kvc_episode_pack(const kvc_block_state* st, void* Kp, void* Vp, int32_t* pos_opt,
+                                    kvc_stream stream);
+
+/* Episode swap: writes the active episode image back (device -> page-locked
+ * host) on out_stream and brings another one in (page-locked host -> device)
+ * on in_stream, so the two directions share the link at the same time.  Each
+ * half is skipped when its byte count is 0.  Host buffers must be page-locked
+ * and device buffers device memory (KVC_ERR_INVALID otherwise).  The copies
+ * are asynchronous; order them against kernels with the streams. */
+KVC_API kvc_status kvc_episode_swap(const void* dev_out, void* host_out, size_t bytes_out, const void* host_in,
+                                    void* dev_in, size_t bytes_in, kvc_stream out_stream, kvc_stream in_stream);
+
 #ifdef __cplusplus
 }
 #endif

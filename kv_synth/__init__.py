@@ -356,3 +356,19 @@ def gen_decode(cfg: DecodeConfig, device="cpu", lens=None, gap: int = 0):
     return dict(K=K, V=V, q=q, rows=rows,
                 seg_off=torch.tensor(off, dtype=torch.int64, device=device),
                 seg_len=torch.tensor(lens, dtype=torch.int32, device=device))
+
+
+# --------------------------------------------------------------------------
+# EpiCache per-turn matching inputs
+# --------------------------------------------------------------------------
+def gen_turn_embeddings(E: int, De: int, B: int, seed: int = 11, spread: float = 0.6, new_topic_frac: float = 0.1):
+    """Episode centroids (N(0, I)) and B question embeddings: most drawn
+    around a random centroid with per-dimension spread `spread`, a fraction
+    `new_topic_frac` drawn far from all of them (3 N(0, I)).  float32."""
+    rng = np.random.default_rng(seed)
+    C = rng.standard_normal((E, De), dtype=np.float32)
+    which = rng.integers(0, E, size=B)
+    Q = C[which] + spread * rng.standard_normal((B, De), dtype=np.float32)
+    far = rng.random(B) < new_topic_frac
+    Q[far] = 3.0 * rng.standard_normal((int(far.sum()), De), dtype=np.float32)
+    return C, Q.astype(np.float32)

@@ -86,6 +86,10 @@ _SIGS = {
                                      c_vp, c_vp, c_sz, c_vp]),
     "kvc_compact_segments": (c_i32, [c_i32, c_i32, ctypes.POINTER(c_i32), ctypes.POINTER(c_i64),
                                      ctypes.POINTER(c_i32)]),
+    "kvc_episode_match": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, ctypes.c_float, c_vp, c_vp, c_vp]),
+    "kvc_episode_rows": (c_i64, [ctypes.POINTER(kvc_block_state)]),
+    "kvc_episode_pack": (c_i32, [ctypes.POINTER(kvc_block_state), c_vp, c_vp, c_vp, c_vp]),
+    "kvc_episode_swap": (c_i32, [c_vp, c_vp, c_sz, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "kvc_profile_begin": (c_i32, []),
     "kvc_profile_end": (c_i32, [ctypes.POINTER(kvc_kernel_time), c_i32, ctypes.POINTER(c_i32)]),
 }
@@ -359,6 +363,41 @@ def kvc_compact_segments(L: int, Hkv: int, k_per_layer) -> tuple[list[int], list
     ln = (c_i32 * (L * Hkv))()
     _check("kvc_compact_segments", lib().kvc_compact_segments(L, Hkv, _i32_array(k_per_layer), off, ln))
     return list(off), list(ln)
+
+
+# ---------------------------------------------------------------- EpiCache per turn
+def kvc_episode_match(queries, centroids, episode, dist2=None, tau=0.0, stream=None) -> None:
+    """Closest episode centroid of each question embedding (-1 past tau)."""
+    B, De = int(queries.shape[0]), int(queries.shape[1])
+    E = int(centroids.shape[0])
+    _check("kvc_episode_match", lib().kvc_episode_match(
+        B, E, De, _dev(queries, torch.float32, "queries"), _dev(centroids, torch.float32, "centroids"), float(tau),
+        _dev(episode, torch.int32, "episode"), _dev(dist2, torch.float32, "dist2"), _stream(stream)))
+
+
+def kvc_episode_rows(st) -> int:
+    return int(lib().kvc_episode_rows(ctypes.byref(st)))
+
+
+def kvc_episode_pack(st, Kp, Vp, pos=None, stream=None) -> None:
+    _check("kvc_episode_pack", lib().kvc_episode_pack(
+        ctypes.byref(st), _dev(Kp, torch.bfloat16, "Kp"), _dev(Vp, torch.bfloat16, "Vp"),
+        _dev(pos, torch.int32, "pos"), _stream(stream)))
+
+
+def kvc_episode_swap(dev_out=None, host_out=None, host_in=None, dev_in=None, out_stream=None, in_stream=None) -> None:
+    """Write dev_out back into pinned host_out and bring pinned host_in into
+    dev_in, on two streams (either pair may be None)."""
+    def ptr(t):
+        return None if t is None else c_vp(t.data_ptr())
+    n_out = 0 if dev_out is None else dev_out.numel() * dev_out.element_size()
+    n_in = 0 if host_in is None else host_in.numel() * host_in.element_size()
+    if dev_out is not None and host_out.numel() * host_out.element_size() != n_out:
+        raise ValueError("host_out must have the size of dev_out")
+    if host_in is not None and dev_in.numel() * dev_in.element_size() != n_in:
+        raise ValueError("dev_in must have the size of host_in")
+    _check("kvc_episode_swap", lib().kvc_episode_swap(ptr(dev_out), ptr(host_out), n_out, ptr(host_in), ptr(dev_in),
+                                                      n_in, _stream(out_stream), _stream(in_stream)))
 
 
 # ---------------------------------------------------------------- EpiCache block prefill

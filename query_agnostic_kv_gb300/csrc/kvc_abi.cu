@@ -856,3 +856,87 @@ kvc_status kvc_compact_segments(int32_t L, int32_t Hkv, const int32_t* k_per_lay
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- EpiCache per-turn path
+namespace {
+
+bool is_pinned_host(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+bool is_device_mem(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvc_status kvc_episode_match(int32_t B, int32_t E, int32_t De, const float* queries, const float* centroids,
+                             float tau, int32_t* episode, float* dist2_opt, kvc_stream stream) {
+  if (B < 0 || E < 1 || De < 4 || De % 4 != 0 || !(tau == tau)) return KVC_ERR_INVALID;
+  if (B == 0) return KVC_OK;
+  if (!queries || !centroids || !episode || !aligned16(queries) || !aligned16(centroids) ||
+      (reinterpret_cast<uintptr_t>(episode) & 3u) || (dist2_opt && (reinterpret_cast<uintptr_t>(dist2_opt) & 3u)))
+    return KVC_ERR_INVALID;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return cuda_status(launch_match(B, E, De, queries, centroids, tau, episode, dist2_opt, cs(stream)));
+}
+
+int64_t kvc_episode_rows(const kvc_block_state* st) {
+  if (!st || st->L < 1 || st->L > kMaxLayers || st->Hkv < 1) return -1;
+  int64_t rows = 0;
+  for (int l = 0; l < st->L; ++l) rows += int64_t(st->Hkv) * st->len[l];
+  return rows;
+}
+
+kvc_status kvc_episode_pack(const kvc_block_state* st, void* Kp, void* Vp, int32_t* pos_opt, kvc_stream stream) {
+  if (kvc_episode_rows(st) < 0 || !Kp || !Vp || !aligned16(Kp) || !aligned16(Vp) || st->d != kHeadDim)
+    return KVC_ERR_INVALID;
+  PackParams pp{};
+  pp.L = st->L;
+  pp.Hkv = st->Hkv;
+  pp.cap = st->capacity;
+  int64_t row = 0;
+  for (int l = 0; l < st->L; ++l) {
+    if (st->len[l] < 0 || st->len[l] > st->capacity || (st->cur[l] != 0 && st->cur[l] != 1)) return KVC_ERR_INVALID;
+    pp.len[l] = st->len[l];
+    pp.cur[l] = st->cur[l];
+    pp.dst_off[l] = row;
+    row += int64_t(st->Hkv) * st->len[l];
+  }
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return cuda_status(launch_pack(st->K[0], st->V[0], st->pos[0], st->K[1], st->V[1], st->pos[1], Kp, Vp, pos_opt,
+                                 pp, cs(stream)));
+}
+
+kvc_status kvc_episode_swap(const void* dev_out, void* host_out, size_t bytes_out, const void* host_in, void* dev_in,
+                            size_t bytes_in, kvc_stream out_stream, kvc_stream in_stream) {
+  if (bytes_out > 0 && (!dev_out || !host_out || !is_device_mem(dev_out) || !is_pinned_host(host_out)))
+    return KVC_ERR_INVALID;
+  if (bytes_in > 0 && (!host_in || !dev_in || !is_pinned_host(host_in) || !is_device_mem(dev_in)))
+    return KVC_ERR_INVALID;
+  if (bytes_out > 0) {
+    cudaError_t e = cudaMemcpyAsync(host_out, dev_out, bytes_out, cudaMemcpyDeviceToHost, cs(out_stream));
+    if (e != cudaSuccess) return KVC_ERR_CUDA;
+  }
+  if (bytes_in > 0) {
+    cudaError_t e = cudaMemcpyAsync(dev_in, host_in, bytes_in, cudaMemcpyHostToDevice, cs(in_stream));
+    if (e != cudaSuccess) return KVC_ERR_CUDA;
+  }
+  return KVC_OK;
+}
+
+}  // extern "C"

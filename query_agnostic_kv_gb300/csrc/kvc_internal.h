@@ -189,4 +189,18 @@ struct DecodeParams {
 };
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
 
+// EpiCache per-turn path: nearest episode centroid per question (tau <= 0: no
+// new-topic threshold), and packing of a block state's kept rows.
+cudaError_t launch_match(int B, int E, int De, const float* q, const float* c, float tau, int32_t* ep, float* d2,
+                         cudaStream_t st);
+struct PackParams {
+  int L, Hkv;
+  int64_t cap;                    // rows per (l, h) in each slab
+  int32_t len[kMaxLayers];
+  int32_t cur[kMaxLayers];
+  int64_t dst_off[kMaxLayers];    // first packed row of layer l
+};
+cudaError_t launch_pack(const void* K0, const void* V0, const int32_t* P0, const void* K1, const void* V1,
+                        const int32_t* P1, void* Kp, void* Vp, int32_t* Pp, const PackParams& pp, cudaStream_t st);
+
 }  // namespace kvc
