@@ -683,7 +683,8 @@ def run_episode(args, rank, world, local_rank):
             "impl": "reference", "metric": EPISODE_METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "epicache-llama3.2-3b-M8k-swap", "L": L, "Hkv": H, "budgets_sum": sum(budgets)},
+            "config": {"workload": "epicache-llama3.2-3b-M8k-swap", "L": L, "Hkv": H, "mean_budget": cfg.mean_budget,
+                       "alpha": cfg.alpha},
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores(), "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
         return
