@@ -14,7 +14,8 @@ quantiser, is:
 
 * a row is one key or value vector of d = 128 bf16 values, split into
   G = 2 groups of 64 consecutive elements;
-* per group, lo = min and hi = max (exact in fp32); the stored offset is lo
+* per group, lo = min (a -0 minimum taken as +0) and hi = max (exact in
+  fp32); the stored offset is lo
   rounded DOWN to bf16 and the stored step is (hi - lo_b) / 15 in fp32
   rounded UP to bf16, so the 16-level grid lo_b + c * s_b (c = 0..15) spans
   the whole group; a constant group stores s_b = 0;
@@ -69,7 +70,7 @@ def encode(X: np.ndarray):
     X = np.ascontiguousarray(X, dtype=np.float32)
     rows = X.shape[0]
     Xg = X.reshape(rows, D // GROUP, GROUP)
-    lo = Xg.min(axis=2)
+    lo = (Xg.min(axis=2) + np.float32(0.0)).astype(np.float32)   # -0 -> +0: a signed zero minimum is not unique
     hi = Xg.max(axis=2)
     lo_b = bf16_round_down(lo)
     s = ((hi - lo_b).astype(np.float32) / np.float32(15.0)).astype(np.float32)
