@@ -368,6 +368,29 @@ KVC_API kvc_status kvc_episode_pack(const kvc_block_state* st, void* Kp, void* V
 KVC_API kvc_status kvc_episode_swap(const void* dev_out, void* host_out, size_t bytes_out, const void* host_in,
                                     void* dev_in, size_t bytes_in, kvc_stream out_stream, kvc_stream in_stream);
 
+/* ------------------------------------------------------------------ Q4 codec
+ * "Agent Memory Below the Prompt: Persistent Q4 KV Cache for Multi-Agent LLM
+ * Inference on Edge Devices", "방법론 및 시스템 설계": each agent's KV cache is
+ * kept 4-bit quantized so that it is loaded back into attention instead of
+ * being recomputed.  The page fixes no format; this one quantises every row
+ * of 128 bf16 values in two groups of 64:
+ *   offset = group min rounded down to bf16 (a -0 minimum counts as +0),
+ *   step   = (group max - offset) / 15 in fp32 rounded up to bf16 (0 for a
+ *            constant group),
+ *   code   = clamp(rint((x - offset) / step), 0, 15) in IEEE fp32 (0 when
+ *            step = 0), two codes per byte, even element in the low nibble;
+ *   decoded value = bf16_rn(fp32(code * step) + offset), no fused multiply-add.
+ * 72 bytes per row instead of 256.  Values must be finite and below 1e37 in
+ * magnitude (larger ranges overflow the step).
+ *   X       device bf16 [rows][128], 16-byte aligned
+ *   codes   uint8 [rows][64]; params bf16 [rows][2][2] = (step, offset) per
+ *           group; both 4-byte aligned
+ * kvc_q4_decode reads codes and params from device memory or page-locked
+ * host memory (read in place across the host link: only the 72 bytes per
+ * row travel) and writes X in device memory. */
+KVC_API kvc_status kvc_q4_encode(int64_t rows, const void* X, void* codes, void* params, kvc_stream stream);
+KVC_API kvc_status kvc_q4_decode(int64_t rows, const void* codes, const void* params, void* X, kvc_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -90,6 +90,8 @@ _SIGS = {
     "kvc_episode_rows": (c_i64, [ctypes.POINTER(kvc_block_state)]),
     "kvc_episode_pack": (c_i32, [ctypes.POINTER(kvc_block_state), c_vp, c_vp, c_vp, c_vp]),
     "kvc_episode_swap": (c_i32, [c_vp, c_vp, c_sz, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "kvc_q4_encode": (c_i32, [c_i64, c_vp, c_vp, c_vp, c_vp]),
+    "kvc_q4_decode": (c_i32, [c_i64, c_vp, c_vp, c_vp, c_vp]),
     "kvc_profile_begin": (c_i32, []),
     "kvc_profile_end": (c_i32, [ctypes.POINTER(kvc_kernel_time), c_i32, ctypes.POINTER(c_i32)]),
 }
@@ -398,6 +400,22 @@ def kvc_episode_swap(dev_out=None, host_out=None, host_in=None, dev_in=None, out
         raise ValueError("dev_in must have the size of host_in")
     _check("kvc_episode_swap", lib().kvc_episode_swap(ptr(dev_out), ptr(host_out), n_out, ptr(host_in), ptr(dev_in),
                                                       n_in, _stream(out_stream), _stream(in_stream)))
+
+
+# ---------------------------------------------------------------- Q4 codec
+def kvc_q4_encode(X, codes, params, stream=None) -> None:
+    """X bf16 [rows, 128] -> codes uint8 [rows, 64], params bf16 [rows, 2, 2]."""
+    rows = int(X.shape[0])
+    _check("kvc_q4_encode", lib().kvc_q4_encode(rows, _dev(X, torch.bfloat16, "X"), _dev(codes, torch.uint8, "codes"),
+                                                _dev(params, torch.bfloat16, "params"), _stream(stream)))
+
+
+def kvc_q4_decode(codes, params, X, stream=None) -> None:
+    """codes/params (device or pinned host) -> X bf16 [rows, 128] on the device."""
+    rows = int(X.shape[0])
+    _check("kvc_q4_decode", lib().kvc_q4_decode(rows, _dev_or_pinned(codes, torch.uint8, "codes"),
+                                                _dev_or_pinned(params, torch.bfloat16, "params"),
+                                                _dev(X, torch.bfloat16, "X"), _stream(stream)))
 
 
 # ---------------------------------------------------------------- EpiCache block prefill

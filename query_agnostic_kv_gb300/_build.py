@@ -14,7 +14,7 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvc.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["kvc_abi.cu", "kvc_proxy.cu", "kvc_topk.cu", "kvc_recon.cu", "kvc_compact.cu", "kvc_noalloc.cu", "kvc_decode.cu", "kvc_episode.cu"]
+SOURCES = ["kvc_abi.cu", "kvc_proxy.cu", "kvc_topk.cu", "kvc_recon.cu", "kvc_compact.cu", "kvc_noalloc.cu", "kvc_decode.cu", "kvc_episode.cu", "kvc_q4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -940,3 +940,30 @@ kvc_status kvc_episode_swap(const void* dev_out, void* host_out, size_t bytes_ou
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- Q4 codec
+extern "C" {
+
+kvc_status kvc_q4_encode(int64_t rows, const void* X, void* codes, void* params, kvc_stream stream) {
+  if (rows < 0) return KVC_ERR_INVALID;
+  if (rows == 0) return KVC_OK;
+  if (!X || !codes || !params || !aligned16(X) || (reinterpret_cast<uintptr_t>(codes) & 3u) ||
+      (reinterpret_cast<uintptr_t>(params) & 3u))
+    return KVC_ERR_INVALID;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return cuda_status(launch_q4_encode(rows, X, codes, params, cs(stream)));
+}
+
+kvc_status kvc_q4_decode(int64_t rows, const void* codes, const void* params, void* X, kvc_stream stream) {
+  if (rows < 0) return KVC_ERR_INVALID;
+  if (rows == 0) return KVC_OK;
+  if (!X || !codes || !params || !aligned16(X) || (reinterpret_cast<uintptr_t>(codes) & 3u) ||
+      (reinterpret_cast<uintptr_t>(params) & 3u))
+    return KVC_ERR_INVALID;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return cuda_status(launch_q4_decode(rows, codes, params, X, cs(stream)));
+}
+
+}  // extern "C"

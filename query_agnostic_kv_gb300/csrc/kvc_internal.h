@@ -200,6 +200,10 @@ struct PackParams {
   int32_t cur[kMaxLayers];
   int64_t dst_off[kMaxLayers];    // first packed row of layer l
 };
+// Q4 codec of bf16 rows of 128 values (codes [rows][64] bytes, params
+// [rows][2] x (step, offset) bf16).
+cudaError_t launch_q4_encode(int64_t rows, const void* X, void* codes, void* params, cudaStream_t st);
+cudaError_t launch_q4_decode(int64_t rows, const void* codes, const void* params, void* X, cudaStream_t st);
 cudaError_t launch_pack(const void* K0, const void* V0, const int32_t* P0, const void* K1, const void* V1,
                         const int32_t* P1, void* Kp, void* Vp, int32_t* Pp, const PackParams& pp, cudaStream_t st);
 

@@ -1,0 +1,132 @@
+// 4-bit (Q4) codec of a compacted KV cache ("Agent Memory Below the Prompt:
+// Persistent Q4 KV Cache for Multi-Agent LLM Inference on Edge Devices",
+// "방법론 및 시스템 설계": each agent's cache is kept 4-bit quantized and loaded
+// straight back into attention).  The page fixes no format; this codec is an
+// affine group quantiser over groups of 64 values of a 128-value row:
+//   offset = min rounded down to bf16, step = (max - offset) / 15 rounded up
+//   to bf16 (0 for a constant group), code = clamp(rint((x - offset) / step),
+//   0, 15), two codes per byte (even element in the low nibble);
+//   decode = bf16_rn(c * step + offset) with separately rounded fp32 ops.
+// Every decision uses IEEE-rounded fp32 intrinsics (no contraction, no fast
+// division), so results are bit-exact with a plain fp32 restatement.
+//
+// Both kernels: 8 lanes per group (one 16-byte load or store of 8 bf16 each),
+// a warp covers 2 rows, grid-stride over rows.  The decoder's inputs may be
+// page-locked host memory read in place (72 bytes per row cross the link,
+// 256 bytes per row are written to HBM).
+#include <cuda_bf16.h>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int ROWS_PER_BLOCK = THREADS / 16;   // 16 lanes per row
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__global__ void __launch_bounds__(THREADS) q4_encode_kernel(int64_t rows, const uint4* __restrict__ X,
+                                                            uint32_t* __restrict__ codes,
+                                                            uint32_t* __restrict__ params) {
+  const int li = threadIdx.x & 7;           // lane within the group
+  const int g = (threadIdx.x >> 3) & 1;     // group within the row
+  const int half = (threadIdx.x >> 4) & 1;  // row of the warp's pair
+  // The loop runs over the warp's row pair, so every lane takes the same
+  // trips and the shuffles below always see the full warp.
+  for (int64_t base = int64_t(blockIdx.x) * ROWS_PER_BLOCK + (threadIdx.x >> 5) * 2; base < rows;
+       base += int64_t(gridDim.x) * ROWS_PER_BLOCK) {
+    const int64_t r = base + half;
+    const bool ok = r < rows;
+    const uint4 w = ok ? X[r * 16 + g * 8 + li] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[2 * k] = bf16_lo(ww[k]);
+      v[2 * k + 1] = bf16_hi(ww[k]);
+    }
+    float mn = v[0], mx = v[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) {
+      mn = fminf(mn, v[k]);
+      mx = fmaxf(mx, v[k]);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    mn = __fadd_rn(mn, 0.f);                  // -0 -> +0: min over {-0, +0} may give either
+    const __nv_bfloat16 lo_h = __float2bfloat16_rd(mn);
+    const float lo = __bfloat162float(lo_h);
+    __nv_bfloat16 s_h = __float2bfloat16_rn(0.f);
+    if (mx != mn) s_h = __float2bfloat16_ru(__fdiv_rn(__fsub_rn(mx, lo), 15.f));
+    const float s = __bfloat162float(s_h);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float t = 0.f;
+      if (s > 0.f) t = __fdiv_rn(__fsub_rn(v[k], lo), s);
+      const float c = fminf(fmaxf(rintf(t), 0.f), 15.f);
+      packed |= static_cast<uint32_t>(c) << (4 * k);
+    }
+    if (!ok) continue;
+    codes[r * 16 + g * 8 + li] = packed;
+    if (li == 0)
+      params[r * 2 + g] = static_cast<uint32_t>(__bfloat16_as_ushort(s_h)) |
+                          (static_cast<uint32_t>(__bfloat16_as_ushort(lo_h)) << 16);
+  }
+}
+
+__global__ void __launch_bounds__(THREADS) q4_decode_kernel(int64_t rows, const uint32_t* __restrict__ codes,
+                                                            const uint32_t* __restrict__ params,
+                                                            uint4* __restrict__ X) {
+  const int li = threadIdx.x & 7;
+  const int g = (threadIdx.x >> 3) & 1;
+  const int rs = threadIdx.x >> 4;
+  for (int64_t r = int64_t(blockIdx.x) * ROWS_PER_BLOCK + rs; r < rows;
+       r += int64_t(gridDim.x) * ROWS_PER_BLOCK) {
+    const uint32_t packed = codes[r * 16 + g * 8 + li];
+    const uint32_t pr = params[r * 2 + g];
+    const float s = bf16_lo(pr);
+    const float lo = bf16_hi(pr);
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float c0 = static_cast<float>((packed >> (8 * k)) & 0xfu);
+      const float c1 = static_cast<float>((packed >> (8 * k + 4)) & 0xfu);
+      const __nv_bfloat16 a = __float2bfloat16_rn(__fadd_rn(__fmul_rn(c0, s), lo));
+      const __nv_bfloat16 b = __float2bfloat16_rn(__fadd_rn(__fmul_rn(c1, s), lo));
+      out[k] = static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+    }
+    X[r * 16 + g * 8 + li] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+int grid_for(int64_t rows) {
+  const int64_t need = (rows + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
+  const int64_t cap = int64_t(num_sms()) * 8;     // 8 blocks of 256 threads per SM
+  return static_cast<int>(need < cap ? need : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_q4_encode(int64_t rows, const void* X, void* codes, void* params, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  ProfScope ps("q4_encode", st);
+  q4_encode_kernel<<<grid_for(rows), THREADS, 0, st>>>(rows, static_cast<const uint4*>(X),
+                                                       static_cast<uint32_t*>(codes), static_cast<uint32_t*>(params));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q4_decode(int64_t rows, const void* codes, const void* params, void* X, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  ProfScope ps("q4_decode", st);
+  q4_decode_kernel<<<grid_for(rows), THREADS, 0, st>>>(rows, static_cast<const uint32_t*>(codes),
+                                                       static_cast<const uint32_t*>(params), static_cast<uint4*>(X));
+  return cudaGetLastError();
+}
+
+}  // namespace kvc
