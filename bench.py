@@ -50,9 +50,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use only this many layers (profiling cases)")
     ap.add_argument("--proxy", choices=["keydiff", "knorm"], default="keydiff", help="stage-1 proxy")
-    ap.add_argument("--op", choices=["compress", "decode", "episode"], default="compress",
+    ap.add_argument("--op", choices=["compress", "decode", "episode", "q4"], default="compress",
                     help="compress: the KV² compression step; decode: attention over the compacted cache; "
-                         "episode: EpiCache per-turn match + episode cache swap")
+                         "episode: EpiCache per-turn match + episode cache swap; q4: Q4 codec of the cache")
     ap.add_argument("--decode-config", default=ks.DECODE_128K.name, choices=list(ks.DECODE_CONFIGS))
     return ap.parse_args()
 
@@ -855,6 +855,119 @@ def run_episode(args, rank, world, local_rank):
         "cpu_baseline": cpu}), flush=True)
 
 
+# ---------------------------------------------------------------- Q4 codec leg
+Q4_METRIC = "Q4 codec of a compacted KV cache: bf16 bytes encoded or restored per second"
+
+
+def run_q4(args, rank, world, local_rank):
+    import torch
+    import query_agnostic_kv_gb300 as qk
+    from query_agnostic_kv_gb300 import _build
+
+    cfg = ks.DECODE_CONFIGS[args.decode_config]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import q4
+        x = ks.gen_decode(cfg, "cpu", lens=[min(cfg.kept, 65536)])
+        X = x["K"].float().numpy()
+        samples = []
+        for i in range(args.warmup + args.steps):
+            a = time.perf_counter()
+            c, s, lo = q4.encode(X)
+            q4.decode(c, s, lo)
+            if i >= args.warmup:
+                samples.append(time.perf_counter() - a)
+        t = statistics.median(samples)
+        v = 2 * X.shape[0] * 256 / t / 1e9
+        desc = f"encode + decode of {X.shape[0]} rows"
+        print(json.dumps({
+            "impl": "reference", "metric": Q4_METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u4", "data": "synthetic",
+            "config": {"workload": cfg.name + "-q4"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _build.build_library()
+    qk.kvc_device_check()
+    x = ks.gen_decode(cfg, dev)
+    X = torch.cat([x["K"], x["V"]])                      # every kept K and V row of one layer of the batch
+    rows = X.shape[0]
+    codes = torch.empty(rows, 64, dtype=torch.uint8, device=dev)
+    params = torch.empty(rows, 2, 2, dtype=torch.bfloat16, device=dev)
+    Y = torch.empty_like(X)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        qk.kvc_q4_encode(X, codes, params)
+        qk.kvc_q4_decode(codes, params, Y)
+    hc, hp = codes.cpu().pin_memory(), params.cpu().pin_memory()
+    assert qk.kvc_stream_status() == 0
+    bf16_bytes = rows * 256
+    q4_bytes = rows * 72
+
+    def timed(fn, n):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    qk.kvc_profile_begin()
+    ms_enc = timed(lambda: qk.kvc_q4_encode(X, codes, params), args.steps)
+    ms_dec = timed(lambda: qk.kvc_q4_decode(codes, params, Y), args.steps)
+    prof = qk.kvc_profile_end()
+    clocks = sampler.stop()
+    # restore from page-locked host memory: the kernel reads the Q4 image in place
+    # across the host link (the sampler is off: its queries stall host-link traffic)
+    ms_rest = timed(lambda: qk.kvc_q4_decode(hc, hp, Y), max(3, args.steps // 4))
+    hX = torch.empty(X.shape, dtype=torch.bfloat16).pin_memory()
+    ms_h2d = timed(lambda: Y.copy_(hX, non_blocking=True), max(3, args.steps // 4))
+    assert qk.kvc_stream_status() == 0
+    hbm = load_peaks()[0].get("hbm_gbs")
+    enc_l, enc_t = prof["q4_encode"]
+    dec_l, dec_t = prof["q4_decode"]
+    traffic = bf16_bytes + q4_bytes                      # one read and one write per row, either direction
+    ach_enc = traffic / (enc_t / enc_l / 1e3) / 1e9
+    ach_dec = traffic / (dec_t / dec_l / 1e3) / 1e9
+    value = 2 * bf16_bytes / ((ms_enc + ms_dec) / 1e3) / 1e9
+    print(json.dumps({
+        "metric": Q4_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_enc + ms_dec, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u4", "data": "synthetic",
+        "config": {"workload": cfg.name + "-q4", "rows": rows, "bf16_bytes": bf16_bytes, "q4_bytes": q4_bytes,
+                   "l2": "inputs larger than L2; no flush between steps", "step": "one encode + one decode"},
+        "roofline": {"kernel": "q4_decode", "bound": "hbm", "achieved": ach_dec, "peak": hbm, "unit": "GB/s",
+                     "frac": ach_dec / hbm, "traffic": None,
+                     "peak_source": "hbm_gbs of measured peaks", "algorithmic_bytes_per_launch": traffic},
+        "encode": {"ms": enc_t / enc_l, "GB/s": ach_enc, "frac_of_hbm": ach_enc / hbm},
+        "decode": {"ms": dec_t / dec_l, "GB/s": ach_dec, "frac_of_hbm": ach_dec / hbm},
+        "restore_from_host": {"ms": ms_rest, "bf16_GB/s": bf16_bytes / (ms_rest / 1e3) / 1e9,
+                              "link_GB/s": q4_bytes / (ms_rest / 1e3) / 1e9,
+                              "bf16_h2d_copy_ms": ms_h2d,
+                              "speedup_vs_bf16_copy": ms_h2d / ms_rest},
+        "kernels": {n: {"launches": v[0], "avg_ms": v[1] / v[0]} for n, v in prof.items()},
+        "gpu_launches": enc_l + dec_l, "clocks": clocks,
+        "e2e": {"value": bf16_bytes / (ms_rest / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q4_bytes,
+                "d2h_bytes_per_step": 0, "ms_per_step": ms_rest,
+                "how": "restore: the Q4 image in page-locked host memory decoded in place into device bf16 rows"},
+        "cpu_baseline": None}), flush=True)
+
+
 def main():
     args = parse()
     cfg = ks.KV2_CONFIGS[args.config]
@@ -868,6 +981,9 @@ def main():
         return
     if args.op == "episode":
         run_episode(args, rank, world, local_rank)
+        return
+    if args.op == "q4":
+        run_q4(args, rank, world, local_rank)
         return
     if args.impl == "reference":
         run_reference(args, cfg, rank, world)

@@ -7,8 +7,9 @@
 //   to bf16 (0 for a constant group), code = clamp(rint((x - offset) / step),
 //   0, 15), two codes per byte (even element in the low nibble);
 //   decode = bf16_rn(c * step + offset) with separately rounded fp32 ops.
-// Every decision uses IEEE-rounded fp32 intrinsics (no contraction, no fast
-// division), so results are bit-exact with a plain fp32 restatement.
+// Every decision uses IEEE-rounded fp32 intrinsics (no contraction), and the
+// code division is resolved exactly (see the encoder), so results are
+// bit-exact with a plain fp32 restatement.
 //
 // Both kernels: 8 lanes per group (one 16-byte load or store of 8 bf16 each),
 // a warp covers 2 rows, grid-stride over rows.  The decoder's inputs may be
@@ -27,56 +28,87 @@ constexpr int ROWS_PER_BLOCK = THREADS / 16;   // 16 lanes per row
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+constexpr int PAIRS = 4;   // row pairs a warp loads before it computes (memory parallelism)
+
+// One group of 64 values held by 8 lanes (8 values each): step, offset and
+// the lane's 8 codes packed into 32 bits.
+__device__ __forceinline__ void encode_group(const uint4 w, uint32_t& packed, uint32_t& param) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  float v[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = bf16_lo(ww[k]);
+    v[2 * k + 1] = bf16_hi(ww[k]);
+  }
+  float mn = v[0], mx = v[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k) {
+    mn = fminf(mn, v[k]);
+    mx = fmaxf(mx, v[k]);
+  }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  mn = __fadd_rn(mn, 0.f);                  // -0 -> +0: min over {-0, +0} may give either
+  const __nv_bfloat16 lo_h = __float2bfloat16_rd(mn);
+  const float lo = __bfloat162float(lo_h);
+  __nv_bfloat16 s_h = __float2bfloat16_rn(0.f);
+  if (mx != mn) s_h = __float2bfloat16_ru(__fdiv_rn(__fsub_rn(mx, lo), 15.f));
+  const float s = __bfloat162float(s_h);
+  // code = rint(RN(a / s)) with a = x - offset in [0, 15 s].  The product
+  // t = RN(a * RN(1/s)) is within 2^-23 |a/s| <= 1.9e-6 of a/s, and RN(a/s)
+  // within 9.3e-7 of it, so unless t lies within 1e-4 of a half-integer
+  // both round to the same integer; inside that window the IEEE quotient
+  // itself is taken.  Subnormal steps (1/s would overflow) always divide.
+  const bool fast = s >= 1.17549435e-38f;              // 2^-126, the smallest normal float
+  const float rs = fast ? __frcp_rn(s) : 0.f;
+  // rint(t) for 0 <= t < 2^22: RN(t + 2^23) holds it, ties to even, in its
+  // low mantissa bits (a >= 0 because the offset is at most the minimum).
+  constexpr float kMagic = 8388608.f;                  // 2^23
+  packed = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float a = __fsub_rn(v[k], lo);
+    const float t = __fmul_rn(a, rs);
+    float m = __fadd_rn(t, kMagic);
+    if (s > 0.f && (!fast || fabsf(__fsub_rn(t, __fsub_rn(m, kMagic))) > 0.4999f))
+      m = __fadd_rn(__fdiv_rn(a, s), kMagic);            // near a half-integer: the IEEE quotient
+    const uint32_t c = min(__float_as_uint(m) & 0x1fu, 15u);
+    packed |= c << (4 * k);
+  }
+  param = static_cast<uint32_t>(__bfloat16_as_ushort(s_h)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo_h)) << 16);
+}
+
 __global__ void __launch_bounds__(THREADS) q4_encode_kernel(int64_t rows, const uint4* __restrict__ X,
                                                             uint32_t* __restrict__ codes,
                                                             uint32_t* __restrict__ params) {
   const int li = threadIdx.x & 7;           // lane within the group
   const int g = (threadIdx.x >> 3) & 1;     // group within the row
-  const int half = (threadIdx.x >> 4) & 1;  // row of the warp's pair
-  // The loop runs over the warp's row pair, so every lane takes the same
-  // trips and the shuffles below always see the full warp.
-  for (int64_t base = int64_t(blockIdx.x) * ROWS_PER_BLOCK + (threadIdx.x >> 5) * 2; base < rows;
-       base += int64_t(gridDim.x) * ROWS_PER_BLOCK) {
-    const int64_t r = base + half;
-    const bool ok = r < rows;
-    const uint4 w = ok ? X[r * 16 + g * 8 + li] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    float v[8];
+  const int half = (threadIdx.x >> 4) & 1;  // row of the pair
+  const int64_t warp_rows = 2 * PAIRS;
+  const int64_t stride = int64_t(gridDim.x) * (THREADS / 32) * warp_rows;
+  // The loop runs over the warp's block of rows, so every lane takes the
+  // same trips and the shuffles always see the full warp.
+  for (int64_t base = (int64_t(blockIdx.x) * (THREADS / 32) + (threadIdx.x >> 5)) * warp_rows; base < rows;
+       base += stride) {
+    uint4 w[PAIRS];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      v[2 * k] = bf16_lo(ww[k]);
-      v[2 * k + 1] = bf16_hi(ww[k]);
-    }
-    float mn = v[0], mx = v[0];
-#pragma unroll
-    for (int k = 1; k < 8; ++k) {
-      mn = fminf(mn, v[k]);
-      mx = fmaxf(mx, v[k]);
+    for (int p = 0; p < PAIRS; ++p) {
+      const int64_t r = base + 2 * p + half;
+      w[p] = r < rows ? X[r * 16 + g * 8 + li] : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int p = 0; p < PAIRS; ++p) {
+      const int64_t r = base + 2 * p + half;
+      uint32_t packed, param;
+      encode_group(w[p], packed, param);
+      if (r < rows) {
+        codes[r * 16 + g * 8 + li] = packed;
+        if (li == 0) params[r * 2 + g] = param;
+      }
     }
-    mn = __fadd_rn(mn, 0.f);                  // -0 -> +0: min over {-0, +0} may give either
-    const __nv_bfloat16 lo_h = __float2bfloat16_rd(mn);
-    const float lo = __bfloat162float(lo_h);
-    __nv_bfloat16 s_h = __float2bfloat16_rn(0.f);
-    if (mx != mn) s_h = __float2bfloat16_ru(__fdiv_rn(__fsub_rn(mx, lo), 15.f));
-    const float s = __bfloat162float(s_h);
-    uint32_t packed = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float t = 0.f;
-      if (s > 0.f) t = __fdiv_rn(__fsub_rn(v[k], lo), s);
-      const float c = fminf(fmaxf(rintf(t), 0.f), 15.f);
-      packed |= static_cast<uint32_t>(c) << (4 * k);
-    }
-    if (!ok) continue;
-    codes[r * 16 + g * 8 + li] = packed;
-    if (li == 0)
-      params[r * 2 + g] = static_cast<uint32_t>(__bfloat16_as_ushort(s_h)) |
-                          (static_cast<uint32_t>(__bfloat16_as_ushort(lo_h)) << 16);
   }
 }
 
@@ -105,8 +137,8 @@ __global__ void __launch_bounds__(THREADS) q4_decode_kernel(int64_t rows, const 
   }
 }
 
-int grid_for(int64_t rows) {
-  const int64_t need = (rows + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
+int grid_for(int64_t rows, int rows_per_block) {
+  const int64_t need = (rows + rows_per_block - 1) / rows_per_block;
   const int64_t cap = int64_t(num_sms()) * 8;     // 8 blocks of 256 threads per SM
   return static_cast<int>(need < cap ? need : cap);
 }
@@ -116,7 +148,7 @@ int grid_for(int64_t rows) {
 cudaError_t launch_q4_encode(int64_t rows, const void* X, void* codes, void* params, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   ProfScope ps("q4_encode", st);
-  q4_encode_kernel<<<grid_for(rows), THREADS, 0, st>>>(rows, static_cast<const uint4*>(X),
+  q4_encode_kernel<<<grid_for(rows, (THREADS / 32) * 2 * PAIRS), THREADS, 0, st>>>(rows, static_cast<const uint4*>(X),
                                                        static_cast<uint32_t*>(codes), static_cast<uint32_t*>(params));
   return cudaGetLastError();
 }
@@ -124,7 +156,7 @@ cudaError_t launch_q4_encode(int64_t rows, const void* X, void* codes, void* par
 cudaError_t launch_q4_decode(int64_t rows, const void* codes, const void* params, void* X, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   ProfScope ps("q4_decode", st);
-  q4_decode_kernel<<<grid_for(rows), THREADS, 0, st>>>(rows, static_cast<const uint32_t*>(codes),
+  q4_decode_kernel<<<grid_for(rows, ROWS_PER_BLOCK), THREADS, 0, st>>>(rows, static_cast<const uint32_t*>(codes),
                                                        static_cast<const uint32_t*>(params), static_cast<uint4*>(X));
   return cudaGetLastError();
 }
