@@ -30,27 +30,33 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 constexpr int PAIRS = 4;   // row pairs a warp loads before it computes (memory parallelism)
 
+// bf16x2 minimum of two packed pairs (exact: a selection per half).
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 r = __hmin2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // One group of 64 values held by 8 lanes (8 values each): step, offset and
 // the lane's 8 codes packed into 32 bits.
 __device__ __forceinline__ void encode_group(const uint4 w, uint32_t& packed, uint32_t& param) {
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-  float v[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    v[2 * k] = bf16_lo(ww[k]);
-    v[2 * k + 1] = bf16_hi(ww[k]);
+  // min and max travel together as the packed pair (min, -max): one bf16x2
+  // minimum updates both, one shuffle moves both
+  uint32_t mm;
+  {
+    const uint32_t m01 = bmin2(ww[0], ww[1]), m23 = bmin2(ww[2], ww[3]);
+    const uint32_t n01 = bmin2(ww[0] ^ 0x80008000u, ww[1] ^ 0x80008000u);
+    const uint32_t n23 = bmin2(ww[2] ^ 0x80008000u, ww[3] ^ 0x80008000u);
+    const uint32_t lo2 = bmin2(m01, m23), nhi2 = bmin2(n01, n23);   // (min, min) and (-max, -max) of the halves
+    const uint32_t a = __byte_perm(lo2, nhi2, 0x5410);              // (lo2.lo, nhi2.lo)
+    const uint32_t b = __byte_perm(lo2, nhi2, 0x7632);              // (lo2.hi, nhi2.hi)
+    mm = bmin2(a, b);
   }
-  float mn = v[0], mx = v[0];
 #pragma unroll
-  for (int k = 1; k < 8; ++k) {
-    mn = fminf(mn, v[k]);
-    mx = fmaxf(mx, v[k]);
-  }
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
+  for (int o = 1; o < 8; o <<= 1) mm = bmin2(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+  float mn = bf16_lo(mm);
+  const float mx = -bf16_hi(mm);
   mn = __fadd_rn(mn, 0.f);                  // -0 -> +0: min over {-0, +0} may give either
   const __nv_bfloat16 lo_h = __float2bfloat16_rd(mn);
   const float lo = __bfloat162float(lo_h);
@@ -67,17 +73,30 @@ __device__ __forceinline__ void encode_group(const uint4 w, uint32_t& packed, ui
   // rint(t) for 0 <= t < 2^22: RN(t + 2^23) holds it, ties to even, in its
   // low mantissa bits (a >= 0 because the offset is at most the minimum).
   constexpr float kMagic = 8388608.f;                  // 2^23
-  packed = 0;
+  float a[8], m[8];
+  bool near = false;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const float a = __fsub_rn(v[k], lo);
-    const float t = __fmul_rn(a, rs);
-    float m = __fadd_rn(t, kMagic);
-    if (s > 0.f && (!fast || fabsf(__fsub_rn(t, __fsub_rn(m, kMagic))) > 0.4999f))
-      m = __fadd_rn(__fdiv_rn(a, s), kMagic);            // near a half-integer: the IEEE quotient
-    const uint32_t c = min(__float_as_uint(m) & 0x1fu, 15u);
-    packed |= c << (4 * k);
+    const float x = (k & 1) ? bf16_hi(ww[k >> 1]) : bf16_lo(ww[k >> 1]);
+    a[k] = __fsub_rn(x, lo);
+    const float t = __fmul_rn(a[k], rs);
+    m[k] = __fadd_rn(t, kMagic);
+    near |= fabsf(__fsub_rn(t, __fsub_rn(m[k], kMagic))) > 0.4999f;
   }
+  near = (near || !fast) && s > 0.f;
+  if (__any_sync(0xffffffffu, near)) {                 // rare: resolve near-ties with the IEEE quotient
+    if (near) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float t = __fmul_rn(a[k], rs);
+        if (!fast || fabsf(__fsub_rn(t, __fsub_rn(m[k], kMagic))) > 0.4999f)
+          m[k] = __fadd_rn(__fdiv_rn(a[k], s), kMagic);
+      }
+    }
+  }
+  packed = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) packed |= min(__float_as_uint(m[k]) & 0x1fu, 15u) << (4 * k);
   param = static_cast<uint32_t>(__bfloat16_as_ushort(s_h)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo_h)) << 16);
 }
 
