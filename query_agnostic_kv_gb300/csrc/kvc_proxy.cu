@@ -23,13 +23,25 @@ namespace cg = cooperative_groups;
 namespace kvc {
 namespace {
 
+#ifndef KVC_KD_CTAS
+#define KVC_KD_CTAS 2
+#endif
+#ifndef KVC_KD_CACHE
+#define KVC_KD_CACHE 256
+#endif
+#ifndef KVC_KD_REVERSE
+#define KVC_KD_REVERSE 1
+#endif
 // 8 CTAs per head, two resident per SM (measured faster than 16-CTA clusters).
 constexpr int CLUSTER = 8;
 constexpr int THREADS = 512;
-constexpr int CTAS_PER_SM = 2;            // two clusters' CTAs share an SM: one loads while the other waits
+constexpr int CTAS_PER_SM = KVC_KD_CTAS;  // two clusters' CTAs share an SM: one loads while the other waits
 constexpr int HALVES = THREADS / 16;      // half-warps per CTA
 constexpr int UNROLL = 8;                 // rows per half-warp in flight per step (64 KB per CTA)
-constexpr int CACHE_ROWS = 256;           // rows of the slice kept in shared memory for pass B (64 KB)
+constexpr int CACHE_ROWS = KVC_KD_CACHE;  // rows of the slice kept in shared memory for pass B
+// Pass B walks the slice backwards: the rows pass A loaded last are the
+// likeliest to still be in L2, and the first rows come from the cache.
+constexpr bool PASS_B_REVERSE = KVC_KD_REVERSE != 0;
 constexpr int SMEM_BYTES = CACHE_ROWS * 256 + HALVES * 128 * 4;
 
 __device__ __forceinline__ void unpack8(const uint4& q, float (&f)[8]) {
@@ -126,7 +138,9 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
   for (int c = 0; c < 8; ++c) uu[c] = U[l16 * 8 + c];
   const float uinv = unorm_inv;
   float* srow = s_out + static_cast<int64_t>(lh) * N;
-  for (int base = i0; base < i1; base += HALVES * UNROLL) {
+  const int nblk = (i1 - i0 + HALVES * UNROLL - 1) / (HALVES * UNROLL);
+  for (int bi = 0; bi < nblk; ++bi) {
+    const int base = i0 + (PASS_B_REVERSE ? nblk - 1 - bi : bi) * HALVES * UNROLL;
     uint4 q[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
