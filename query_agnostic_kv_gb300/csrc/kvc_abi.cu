@@ -212,7 +212,7 @@ KV2Workspace carve_kv2(const kvc_shape& s, const ChunkPlan& plan, void* base, si
   w.rw.Rpad = recon_rows(G, plan.n_chunks, plan.nq_full, plan.nq_last);
   w.rw.Qg = c.take<uint16_t>(LH * w.rw.Rpad * kHeadDim);
   w.rw.Kg = c.take<uint16_t>(LH * plan.Q * kHeadDim);
-  w.rw.lse2 = c.take<float>(LH * w.rw.Rpad);
+  w.rw.lse2 = c.take<float>(LH * w.rw.Rpad + 256);   // + tail read by 256-row pass-2 lse copies
   w.bytes = ((c.used + 255) & ~size_t(255)) + 256;
   w.ok = c.ok;
   return w;
@@ -622,7 +622,7 @@ BlockWorkspace carve_block(const kvc_block_state* st, int32_t P, void* base, siz
   w.rw.Rpad = recon_rows(G, 1, P, P);
   w.rw.Qg = c.take<uint16_t>(LH * w.rw.Rpad * kHeadDim);
   w.rw.Kg = nullptr;
-  w.rw.lse2 = c.take<float>(LH * w.rw.Rpad);
+  w.rw.lse2 = c.take<float>(LH * w.rw.Rpad + 256);   // + tail read by 256-row pass-2 lse copies
   w.bytes = ((c.used + 255) & ~size_t(255)) + 256;
   w.ok = c.ok;
   return w;

@@ -43,8 +43,8 @@ namespace {
 constexpr int TILE_ROWS = 128;                  // rows of an A tile (TMEM lanes)
 constexpr int TILE_BYTES = TILE_ROWS * 256;     // 128 rows x 128 bf16
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int LSE_STAGE_BYTES = 128 * 4;        // pass 2: lse2 of the B tile's 128 query rows
 constexpr int MAX_KST = 4;
+constexpr int LSE_PAD = 256;                    // lse2 tail padding (floats): pass-2 bulk copies of a last tile
 
 // Per-pass shape of the pipeline.  B tiles of 256 rows (MMA N = 256) halve
 // the A-operand re-reads from shared memory per FLOP; with N = 128 the
@@ -61,18 +61,33 @@ struct Cfg<1> {
   static constexpr int KST = 2;         // B-tile ring depth
   static constexpr bool A_TMEM = false; // A read by the MMA from shared memory
 };
-// Pass 2 keeps its two key tiles in TMEM (copied from a shared-memory
-// staging buffer once per unit, double-buffered in TMEM), so every MMA reads
-// only the 128-row query tile from shared memory.
+// Pass 2: two 128-key A tiles per unit against 256-query B tiles (MMA
+// N = 256), one consumer group per accumulator reading its 256 columns in four
+// 64-column loads (the accumulator is released after the fourth).  Measured
+// against 128-query tiles with the key tiles in TMEM (A_TMEM, still
+// selectable) and against two 128-column consumer groups per accumulator
+// (CSPLIT = 2, whose end-of-unit merge path remains): this shape was fastest.
+#ifndef KVC_P2_BN
+#define KVC_P2_BN 256
+#endif
+#ifndef KVC_P2_CSPLIT
+#define KVC_P2_CSPLIT 1
+#endif
+#ifndef KVC_P2_KST
+#define KVC_P2_KST 2
+#endif
+#ifndef KVC_P2_ATMEM
+#define KVC_P2_ATMEM 0
+#endif
 template <>
 struct Cfg<2> {
   static constexpr int NA = 2;
   static constexpr int ABUF = 1;
   static constexpr int DBUF = 1;
-  static constexpr int BN = 128;
-  static constexpr int CSPLIT = 1;
-  static constexpr int KST = 4;
-  static constexpr bool A_TMEM = true;
+  static constexpr int BN = KVC_P2_BN;
+  static constexpr int CSPLIT = KVC_P2_CSPLIT;
+  static constexpr int KST = KVC_P2_KST;
+  static constexpr bool A_TMEM = KVC_P2_ATMEM != 0;
 };
 constexpr uint32_t TMEM_A_BASE = 256;  // pass 2: A buffers at TMEM columns [256, 512), 64 columns per tile
 template <int PASS>
@@ -84,11 +99,16 @@ constexpr int kBStage = Cfg<PASS>::BN * 256;
 template <int PASS>
 constexpr int kCombBytes = Cfg<PASS>::CSPLIT > 1 ? Cfg<PASS>::NA * TILE_ROWS * 8 : 0;
 template <int PASS>
-constexpr int kSmemBytes = 1024 + kABytes<PASS> + Cfg<PASS>::KST * (kBStage<PASS> + LSE_STAGE_BYTES) +
+constexpr int kLseStage = PASS == 2 ? Cfg<PASS>::BN * 4 : 0;   // pass 2: lse2 of the B tile's query rows
+template <int PASS>
+constexpr int kSmemBytes = 1024 + kABytes<PASS> + Cfg<PASS>::KST * (kBStage<PASS> + kLseStage<PASS>) +
                            kCombBytes<PASS> + 256;
 static_assert(Cfg<1>::NA * Cfg<1>::DBUF * Cfg<1>::BN <= TMEM_COLS, "TMEM pass 1");
-static_assert(Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_A_BASE && TMEM_A_BASE + 2 * Cfg<2>::NA * 64 <= TMEM_COLS,
+static_assert(Cfg<2>::A_TMEM ? (Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_A_BASE &&
+                                TMEM_A_BASE + 2 * Cfg<2>::NA * 64 <= TMEM_COLS)
+                             : Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_COLS,
               "TMEM pass 2");
+static_assert(Cfg<2>::BN <= LSE_PAD, "lse2 padding covers a pass-2 tile");
 static_assert(kSmemBytes<1> <= 232448 && kSmemBytes<2> <= 232448, "shared memory budget of one CTA");
 static_assert(Cfg<1>::KST <= MAX_KST && Cfg<2>::KST <= MAX_KST, "ring depth");
 
@@ -416,9 +436,10 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;                              // [ABUF][NA] tiles
   uint8_t* sB = smem + kABytes<PASS>;              // [KST] tiles of BN rows
-  float* sL = reinterpret_cast<float*>(sB + KST * BSTAGE);                      // [KST][128] (pass 2)
-  float2* sComb = reinterpret_cast<float2*>(sB + KST * (BSTAGE + LSE_STAGE_BYTES));  // [NA][128] (pass 1)
-  Bars* bars = reinterpret_cast<Bars*>(sB + KST * (BSTAGE + LSE_STAGE_BYTES) + kCombBytes<PASS>);
+  constexpr int LSE_STAGE = kLseStage<PASS>;
+  float* sL = reinterpret_cast<float*>(sB + KST * BSTAGE);                      // [KST][BN] (pass 2)
+  float2* sComb = reinterpret_cast<float2*>(sB + KST * (BSTAGE + LSE_STAGE));  // [NA][128] column-half hand-off
+  Bars* bars = reinterpret_cast<Bars*>(sB + KST * (BSTAGE + LSE_STAGE) + kCombBytes<PASS>);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -495,7 +516,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         for (int i = 0; i < U.nT; ++i) {
           if (*abort_flag) break;
           if (!mbar_wait(&bars->b_empty[s], bph ^ 1, P.limit_ns)) { fail(); break; }
-          mbar_arrive_expect_tx(&bars->b_full[s], PASS == 2 ? BSTAGE + LSE_STAGE_BYTES : BSTAGE);
+          mbar_arrive_expect_tx(&bars->b_full[s], BSTAGE + LSE_STAGE);
           const CUtensorMap* map;
           int32_t y;
           if (PASS == 1) {
@@ -510,7 +531,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           } else {
             map = &tmQg;
             y = U.lh * P.Rpad + U.r * P.CR + i * BN;
-            bulk_load(sL + s * 128, P.lse2 + y, LSE_STAGE_BYTES, &bars->b_full[s]);
+            bulk_load(sL + s * BN, P.lse2 + y, LSE_STAGE, &bars->b_full[s]);
           }
           uint8_t* dst = sB + s * BSTAGE;
           tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
@@ -628,7 +649,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         const int j = valid ? local - g * nq : 0;
         float mrun = -INFINITY, ssum = 0.f;
         constexpr int COLS = BN / CSPLIT;  // columns of the tile this warp reads
-        static_assert(COLS == 128, "pass-1 consumers read 128 columns per tile");
+        static_assert(PASS != 1 || COLS == 128, "pass-1 consumers read 128 columns per tile");
         for (int i = 0; i < U.nT; ++i) {
           uint64_t* df = &bars->d_full[db * NA + wg];
           if (!mbar_wait(df, dph, P.limit_ns)) { fail(); break; }
@@ -692,46 +713,82 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           }
         }
       } else {
-        // ---- column max over the chunk's queries for one key per thread
+        // ---- column max over the chunk's queries: one key (TMEM lane) per
+        // thread, this group's half of the accumulator's query columns
+        constexpr int COLS = BN / CSPLIT;
+        static_assert(COLS % 64 == 0, "pass-2 consumers read whole 64-column blocks");
         const int pos = U.key0 + wg * TILE_ROWS + row;
         const bool valid = has_tile && pos < U.hi;
+        const int rows_q = P.G * nq_of(P, U.ai, U.r);    // query rows of this chunk
         float vmax = -INFINITY;
         const uint64_t cc = pack2(c, c);
         for (int i = 0; i < U.nT; ++i) {
           uint64_t* df = &bars->d_full[db * NA + wg];
           if (!mbar_wait(df, dph, P.limit_ns)) { fail(); break; }
           tc_fence_after();
-          float v[128];
-          __syncwarp();
-          tmem_ld128(lane_addr + (db * NA + wg) * BN, v);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
-          if (++db == DBUF) { db = 0; dph ^= 1; }
           // the tile's lse2 row arrived with the B tile (already complete
           // when the MMA ran; this acquires it for this warp)
           if (!mbar_wait(&bars->b_full[cs], cph, P.limit_ns)) { fail(); break; }
-          const float4* l4 = reinterpret_cast<const float4*>(sL + cs * TILE_ROWS);
+          // columns past the chunk's query rows belong to the next chunk
+          const int lim = rows_q - i * BN - chalf * COLS;
+          const float* lrow = sL + cs * BN + chalf * COLS;
+          const uint32_t col = lane_addr + (db * NA + wg) * BN + chalf * COLS;
           float t[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) t[q] = -INFINITY;
 #pragma unroll
-          for (int k4 = 0; k4 < 32; ++k4) {
-            const float4 l = l4[k4];
-            float x0, x1, x2, x3;
-            unpack2(fma2(pack2(v[4 * k4], v[4 * k4 + 1]), cc, pack2(-l.x, -l.y)), x0, x1);
-            unpack2(fma2(pack2(v[4 * k4 + 2], v[4 * k4 + 3]), cc, pack2(-l.z, -l.w)), x2, x3);
-            t[(2 * k4) & 7] = fmax3(t[(2 * k4) & 7], x0, x1);
-            t[(2 * k4 + 1) & 7] = fmax3(t[(2 * k4 + 1) & 7], x2, x3);
+          for (int blk = 0; blk < COLS / 64; ++blk) {
+            float v[64];
+            __syncwarp();
+            tmem_ld64(col + blk * 64, v);
+            if (blk == COLS / 64 - 1) {
+              // the accumulator goes back to the MMA warp once it is in registers
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
+            }
+            const int bl = lim - blk * 64;
+            if (bl <= 0) continue;
+            if (bl < 64) {
+#pragma unroll
+              for (int k = 0; k < 64; ++k) v[k] = (k < bl) ? v[k] : -INFINITY;
+            }
+            const float4* l4 = reinterpret_cast<const float4*>(lrow + blk * 64);
+#pragma unroll
+            for (int k4 = 0; k4 < 16; ++k4) {
+              const float4 l = l4[k4];
+              float x0, x1, x2, x3;
+              unpack2(fma2(pack2(v[4 * k4], v[4 * k4 + 1]), cc, pack2(-l.x, -l.y)), x0, x1);
+              unpack2(fma2(pack2(v[4 * k4 + 2], v[4 * k4 + 3]), cc, pack2(-l.z, -l.w)), x2, x3);
+              t[(2 * k4) & 7] = fmax3(t[(2 * k4) & 7], x0, x1);
+              t[(2 * k4 + 1) & 7] = fmax3(t[(2 * k4 + 1) & 7], x2, x3);
+            }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->b_empty[cs]);
           if (++cs == KST) { cs = 0; cph ^= 1; }
+          if (++db == DBUF) { db = 0; dph ^= 1; }
           vmax = fmax3(vmax, fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]));
           vmax = fmax3(vmax, t[6], t[7]);
         }
         if (*abort_flag) break;
-        if (valid) P.score[static_cast<int64_t>(U.lh) * P.ldS + pos] = ex2(vmax);
+        if (CSPLIT > 1) {
+          // merge the column halves of this key's maximum into chalf 0
+          if (chalf == 1) {
+            if (!mbar_wait(&bars->comb_empty[wg], comb_ph ^ 1, P.limit_ns)) { fail(); break; }
+            sComb[wg * TILE_ROWS + row].x = vmax;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->comb_full[wg]);
+          } else {
+            if (!mbar_wait(&bars->comb_full[wg], comb_ph, P.limit_ns)) { fail(); break; }
+            const float o = sComb[wg * TILE_ROWS + row].x;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->comb_empty[wg]);
+            vmax = fmaxf(vmax, o);
+          }
+          comb_ph ^= 1;
+        }
+        if (chalf == 0 && valid) P.score[static_cast<int64_t>(U.lh) * P.ldS + pos] = ex2(vmax);
       }
     }
   }
@@ -853,7 +910,7 @@ size_t recon_ws_bytes(int L, int Hkv, int G, int n_chunks, int nq_full, int nq_l
   auto add = [&](size_t bytes) { b = ((b + 255) & ~size_t(255)) + bytes; };
   add(static_cast<size_t>(L) * Hkv * Rpad * kHeadDim * 2);            // Qg
   if (need_kg) add(static_cast<size_t>(L) * Hkv * Q * kHeadDim * 2);  // Kg
-  add(static_cast<size_t>(L) * Hkv * Rpad * 4);                        // lse2
+  add((static_cast<size_t>(L) * Hkv * Rpad + LSE_PAD) * 4);            // lse2 (+ tail read by pass-2 bulk copies)
   return b + 256;
 }
 
@@ -903,10 +960,11 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   // Rows are addressed by model layer index, so the maps span all L layers.
   // Pass 1 streams keys in B tiles of Cfg<1>::BN rows; pass 2 reads keys as
   // 128-row A tiles and query rows as 128-row B tiles.
-  CUtensorMap tmQg, tmK0a, tmK1a, tmK0b, tmK1b, tmApp;
+  CUtensorMap tmQg, tmQgB, tmK0a, tmK1a, tmK0b, tmK1b, tmApp;
   const uint64_t LH = static_cast<uint64_t>(pr.L) * pr.Hkv;
   const void* k1 = pr.K[1] ? pr.K[1] : pr.K[0];
   if (!make_tmap_rows(&tmQg, ws.Qg, LH * Rpad, TILE_ROWS)) return cudaErrorInvalidValue;
+  if (!make_tmap_rows(&tmQgB, ws.Qg, LH * Rpad, Cfg<2>::BN)) return cudaErrorInvalidValue;
   if (!make_tmap_rows(&tmK0a, pr.K[0], LH * pr.ldK, TILE_ROWS)) return cudaErrorInvalidValue;
   if (!make_tmap_rows(&tmK1a, k1, LH * pr.ldK, TILE_ROWS)) return cudaErrorInvalidValue;
   if (!make_tmap_rows(&tmK0b, pr.K[0], LH * pr.ldK, Cfg<1>::BN)) return cudaErrorInvalidValue;
@@ -960,7 +1018,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   kp.n_units = acc;
   if (kp.n_units > 0) {
     ProfScope ps("recon_colmax", st);
-    recon_kernel<2><<<kp.n_units < sms ? kp.n_units : sms, kThreads<2>, kSmemBytes<2>, st>>>(tmQg, tmK0a, tmK1a,
+    recon_kernel<2><<<kp.n_units < sms ? kp.n_units : sms, kThreads<2>, kSmemBytes<2>, st>>>(tmQgB, tmK0a, tmK1a,
                                                                                             tmApp, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
