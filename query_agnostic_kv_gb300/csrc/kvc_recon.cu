@@ -49,6 +49,9 @@ constexpr int LSE_PAD = 256;                    // lse2 tail padding (floats): p
 // Per-pass shape of the pipeline.  B tiles of 256 rows (MMA N = 256) halve
 // the A-operand re-reads from shared memory per FLOP; with N = 128 the
 // shared-memory operand traffic, not the tensor core, caps the MMA rate.
+#ifndef KVC_P1_CSPLIT
+#define KVC_P1_CSPLIT 2
+#endif
 template <int PASS>
 struct Cfg;
 template <>
@@ -57,7 +60,7 @@ struct Cfg<1> {
   static constexpr int ABUF = 1;        // A buffers in shared memory
   static constexpr int DBUF = 1;        // accumulator buffers per A tile
   static constexpr int BN = 256;        // rows (keys) of a B tile = MMA N
-  static constexpr int CSPLIT = 2;      // consumer warps sharing one TMEM lane quarter (column split)
+  static constexpr int CSPLIT = KVC_P1_CSPLIT;  // consumer warps sharing one TMEM lane quarter (column split)
   static constexpr int KST = 2;         // B-tile ring depth
   static constexpr bool A_TMEM = false; // A read by the MMA from shared memory
 };
@@ -649,7 +652,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         const int j = valid ? local - g * nq : 0;
         float mrun = -INFINITY, ssum = 0.f;
         constexpr int COLS = BN / CSPLIT;  // columns of the tile this warp reads
-        static_assert(PASS != 1 || COLS == 128, "pass-1 consumers read 128 columns per tile");
+        static_assert(COLS % 64 == 0, "consumers read whole 64-column blocks");
         for (int i = 0; i < U.nT; ++i) {
           uint64_t* df = &bars->d_full[db * NA + wg];
           if (!mbar_wait(df, dph, P.limit_ns)) { fail(); break; }
@@ -658,22 +661,19 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           const int lim = ((tr.kind == 0) ? U.n - tr.t0 : ((tr.chunk == rr) ? (j - tr.t0 + 1) : 0)) -
                           chalf * COLS;
           const uint32_t col = lane_addr + (db * NA + wg) * BN + chalf * COLS;
-          // two 64-column blocks; the accumulator is handed back to the MMA
-          // warp right after the second block is in registers
-          {
+          // 64-column blocks; the accumulator is handed back to the MMA warp
+          // right after the last block is in registers
+#pragma unroll
+          for (int blk = 0; blk < COLS / 64; ++blk) {
             float v[64];
             __syncwarp();
-            tmem_ld64(col, v);
-            row_update<64>(v, lim, c, mrun, ssum);
-          }
-          {
-            float v[64];
-            __syncwarp();
-            tmem_ld64(col + 64, v);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
-            row_update<64>(v, lim - 64, c, mrun, ssum);
+            tmem_ld64(col + blk * 64, v);
+            if (blk == COLS / 64 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
+            }
+            row_update<64>(v, lim - blk * 64, c, mrun, ssum);
           }
           if (++db == DBUF) { db = 0; dph ^= 1; }
         }
