@@ -50,9 +50,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use only this many layers (profiling cases)")
     ap.add_argument("--proxy", choices=["keydiff", "knorm"], default="keydiff", help="stage-1 proxy")
-    ap.add_argument("--op", choices=["compress", "decode", "episode", "q4"], default="compress",
+    ap.add_argument("--op", choices=["compress", "decode", "episode", "q4", "epicache"], default="compress",
                     help="compress: the KV² compression step; decode: attention over the compacted cache; "
-                         "episode: EpiCache per-turn match + episode cache swap; q4: Q4 codec of the cache")
+                         "episode: EpiCache per-turn match + episode cache swap; q4: Q4 codec of the cache; "
+                         "epicache: EpiCache block prefill of every episode")
     ap.add_argument("--decode-config", default=ks.DECODE_128K.name, choices=list(ks.DECODE_CONFIGS))
     return ap.parse_args()
 
@@ -968,6 +969,117 @@ def run_q4(args, rank, world, local_rank):
         "cpu_baseline": None}), flush=True)
 
 
+# ---------------------------------------------------------------- EpiCache block prefill leg
+EPI_METRIC = "EpiCache block prefill: history tokens/s over all episodes (E * N_hist / T)"
+
+
+def run_epicache(args, rank, world, local_rank):
+    import torch
+    import query_agnostic_kv_gb300 as qk
+    from query_agnostic_kv_gb300 import _build
+
+    cfg = ks.EPI_3B
+    L, H, Hq, B, P, S = cfg.L, cfg.Hkv, cfg.Hq, cfg.block, cfg.prompt_len, cfg.sinks
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import kv2
+        budgets = kv2.layer_budgets(ks.gen_sensitivity(cfg).astype(np.float64), cfg.alpha, cfg.mean_budget, S)
+        Kh, Vh = ks.gen_epi_history_layer(cfg, 0)
+        Qp, Kp = ks.gen_epi_prompt_layer(cfg, 0, 0)
+        n = min(cfg.n_hist, 8 * B)
+        a = time.perf_counter()
+        kv2.block_prefill_layer(kv2.bf16_to_f64(Kh[:1, :n]), kv2.bf16_to_f64(Vh[:1, :n]),
+                                kv2.bf16_to_f64(Qp[:cfg.G]), kv2.bf16_to_f64(Kp[:1]), B, int(budgets[0]), S)
+        t = (time.perf_counter() - a) * (cfg.n_hist / n) * L * H      # one KV head of one layer, scaled
+        v = cfg.episodes * cfg.n_hist / (t * cfg.episodes)
+        print(json.dumps({
+            "impl": "reference", "metric": EPI_METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": 1, "warmup": 0, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": cfg.name},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                             "sample": f"layer 0, KV head 0, first {n} history tokens, scaled to {L} layers x {H} "
+                                       f"heads x {cfg.n_hist} tokens"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _build.build_library()
+    qk.kvc_device_check()
+    budgets = qk.kvc_layer_budgets(ks.gen_sensitivity(cfg).tolist(), cfg.alpha, cfg.mean_budget, S)
+    nb = (cfg.n_hist + B - 1) // B
+    # history, block-major on the device: blocks[b] = [L][H][B][d] (last block ragged)
+    Kblk = torch.zeros(nb, L, H, B, 128, dtype=torch.bfloat16, device=dev)
+    Vblk = torch.zeros_like(Kblk)
+    for l in range(L):
+        kh, vh = ks.gen_epi_history_layer(cfg, l)
+        for src, dst in ((kh, Kblk), (vh, Vblk)):
+            t = torch.from_numpy(src.view(np.int16)).view(torch.bfloat16)        # [H][n_hist][d]
+            pad = torch.zeros(H, nb * B - cfg.n_hist, 128, dtype=torch.bfloat16)
+            t = torch.cat([t, pad], dim=1).view(H, nb, B, 128).permute(1, 0, 2, 3)
+            dst[:, l] = t.to(dev)
+    prompts = []
+    for e in range(cfg.episodes):
+        prm = [ks.gen_epi_prompt_layer(cfg, e, l) for l in range(L)]
+        dq = torch.from_numpy(np.stack([p[0] for p in prm]).view(np.int16)).view(torch.bfloat16).to(dev)
+        dk = torch.from_numpy(np.stack([p[1] for p in prm]).view(np.int16)).view(torch.bfloat16).to(dev)
+        prompts.append((dq, dk))
+    cap = max(budgets) + B
+    slabs = [torch.zeros(L * H * cap * 128, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    pos = [torch.zeros(L * H * cap, dtype=torch.int32, device=dev) for _ in range(2)]
+    stream = torch.cuda.current_stream()
+    blocks = [(Kblk[b] if b < nb - 1 or cfg.n_hist % B == 0 else Kblk[b, :, :, :cfg.n_hist - b * B].contiguous(),
+               Vblk[b] if b < nb - 1 or cfg.n_hist % B == 0 else Vblk[b, :, :, :cfg.n_hist - b * B].contiguous(),
+               min(B, cfg.n_hist - b * B)) for b in range(nb)]
+
+    def episode(e, ws=None):
+        st = qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0], slabs[2], slabs[3],
+                                     pos[1])
+        if ws is None:
+            ws = torch.empty(qk.kvc_block_workspace_size(st, B, P), dtype=torch.uint8, device=dev)
+        dq, dk = prompts[e]
+        for kb, vb, n in blocks:
+            qk.kvc_block_prefill_step(st, kb, vb, n, dq, dk, P, ws=ws, stream=stream)
+        return ws
+
+    ws = episode(0)
+    torch.cuda.synchronize()
+    assert qk.kvc_stream_status() == 0
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    qk.kvc_profile_begin()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for e in range(cfg.episodes):
+        episode(e, ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    prof = qk.kvc_profile_end()
+    clocks = sampler.stop()
+    assert qk.kvc_stream_status() == 0
+    ms = a.elapsed_time(b)
+    value = world * cfg.episodes * cfg.n_hist / (ms / 1e3)
+    total = sum(v[1] for v in prof.values())
+    kernels = {n: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / total} for n, v in prof.items()}
+    cpu = None
+    print(json.dumps({
+        "metric": EPI_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": cfg.episodes,
+        "warmup": 1, "ms_per_step": ms / cfg.episodes, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "L": L, "Hkv": H, "Hq": Hq, "n_hist": cfg.n_hist, "block": B,
+                   "episodes": cfg.episodes, "prompt_queries": P, "mean_budget": cfg.mean_budget, "alpha": cfg.alpha,
+                   "step": "one episode (all history blocks)", "l2": "history 10 GB on the device"},
+        "roofline": None, "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()), "clocks": clocks,
+        "e2e": None, "cpu_baseline": cpu}), flush=True)
+
+
 def main():
     args = parse()
     cfg = ks.KV2_CONFIGS[args.config]
@@ -984,6 +1096,9 @@ def main():
         return
     if args.op == "q4":
         run_q4(args, rank, world, local_rank)
+        return
+    if args.op == "epicache":
+        run_epicache(args, rank, world, local_rank)
         return
     if args.impl == "reference":
         run_reference(args, cfg, rank, world)
