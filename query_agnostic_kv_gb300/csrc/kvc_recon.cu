@@ -54,14 +54,23 @@ constexpr int LSE_PAD = 256;                    // lse2 tail padding (floats): p
 #endif
 template <int PASS>
 struct Cfg;
+#ifndef KVC_P1_BN
+#define KVC_P1_BN 256
+#endif
+#ifndef KVC_P1_DBUF
+#define KVC_P1_DBUF 1
+#endif
+#ifndef KVC_P1_KST
+#define KVC_P1_KST 2
+#endif
 template <>
 struct Cfg<1> {
   static constexpr int NA = 2;          // A tiles (128 query rows each) per unit
   static constexpr int ABUF = 1;        // A buffers in shared memory
-  static constexpr int DBUF = 1;        // accumulator buffers per A tile
-  static constexpr int BN = 256;        // rows (keys) of a B tile = MMA N
+  static constexpr int DBUF = KVC_P1_DBUF;  // accumulator buffers per A tile
+  static constexpr int BN = KVC_P1_BN;  // rows (keys) of a B tile = MMA N
   static constexpr int CSPLIT = KVC_P1_CSPLIT;  // consumer warps sharing one TMEM lane quarter (column split)
-  static constexpr int KST = 2;         // B-tile ring depth
+  static constexpr int KST = KVC_P1_KST;  // B-tile ring depth
   static constexpr bool A_TMEM = false; // A read by the MMA from shared memory
 };
 // Pass 2: two 128-key A tiles per unit against 256-query B tiles (MMA
