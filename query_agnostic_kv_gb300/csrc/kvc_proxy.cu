@@ -37,7 +37,10 @@ constexpr int CLUSTER = 8;
 constexpr int THREADS = 512;
 constexpr int CTAS_PER_SM = KVC_KD_CTAS;  // two clusters' CTAs share an SM: one loads while the other waits
 constexpr int HALVES = THREADS / 16;      // half-warps per CTA
-constexpr int UNROLL = 8;                 // rows per half-warp in flight per step (64 KB per CTA)
+#ifndef KVC_KD_UNROLL
+#define KVC_KD_UNROLL 8
+#endif
+constexpr int UNROLL = KVC_KD_UNROLL;      // rows per half-warp in flight per step (64 KB per CTA at 8)
 constexpr int CACHE_ROWS = KVC_KD_CACHE;  // rows of the slice kept in shared memory for pass B
 // Pass B walks the slice backwards: the rows pass A loaded last are the
 // likeliest to still be in L2, and the first rows come from the cache.
