@@ -92,6 +92,13 @@ def algorithmic_work(cfg):
             "bytes": b, "flops_lse_per_launch": f_lse, "flops_colmax_per_launch": f_col}
 
 
+# DRAM bytes per launch of the row-LSE kernel as ncu counted them on the
+# 4-layer case of the 16K workload (dram__bytes_read + dram__bytes_write =
+# 202.27 + 4.10 MB); the traffic grows with the number of (layer, KV head)
+# pairs.  Reset to None whenever the kernel changes until it is captured again.
+LSE_TRAFFIC_PER_LAYER = (202.27e6 + 4.10e6) / 4
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -352,8 +359,12 @@ def run_ours(args, cfg, rank, world, local_rank):
     peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
     ach_lse = work["flops_lse_per_launch"] / lse_avg_s / 1e12
     ach_col = work["flops_colmax_per_launch"] / col_avg_s / 1e12
+    traffic = None
+    if LSE_TRAFFIC_PER_LAYER is not None and cfg.N == ks.LLAMA_16K.N and cfg.Hkv == ks.LLAMA_16K.Hkv:
+        traffic = LSE_TRAFFIC_PER_LAYER * cfg.L
     roof = {"kernel": "recon_lse (tcgen05 row-LSE pass)", "bound": "tensor", "achieved": ach_lse,
-            "peak": peak_tf, "unit": "TFLOP/s", "frac": ach_lse / peak_tf, "traffic": None,
+            "peak": peak_tf, "unit": "TFLOP/s", "frac": ach_lse / peak_tf, "traffic": traffic,
+            "traffic_source": "ncu dram bytes of the 4-layer case, scaled by layers",
             "peak_source": f"bf16_tflops_sustained of {peak_src} peaks",
             "algorithmic_flops_per_launch": work["flops_lse_per_launch"]}
     hbm = peaks.get("hbm_gbs")
