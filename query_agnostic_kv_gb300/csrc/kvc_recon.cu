@@ -365,19 +365,29 @@ __device__ __forceinline__ void lse_update(float (&v)[N], int lim, float c, floa
   ssum += s0 + s1;
 }
 
+#ifndef KVC_SUM_CHAINS
+#define KVC_SUM_CHAINS 8
+#endif
 // Sum of 2^(v*c - m) over N logits (masked entries are -inf and add 0).
 template <int N>
 __device__ __forceinline__ float exp2_sum(const float (&v)[N], float c, float m) {
+  constexpr int CH = KVC_SUM_CHAINS;                    // independent packed partial sums
   const uint64_t cc = pack2(c, c), nm = pack2(-m, -m);
-  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+  uint64_t acc[CH];
+#pragma unroll
+  for (int q = 0; q < CH; ++q) acc[q] = 0ull;
 #pragma unroll
   for (int k = 0; k < N / 2; ++k) {
     float x0, x1;
     unpack2(fma2(pack2(v[2 * k], v[2 * k + 1]), cc, nm), x0, x1);
     const uint64_t e = (k < EMU_PAIRS) ? exp2_poly2(x0, x1) : pack2(ex2(x0), ex2(x1));
-    acc[k & 3] = add2(acc[k & 3], e);
+    acc[k % CH] = add2(acc[k % CH], e);
   }
-  const uint64_t s2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+#pragma unroll
+  for (int w = CH / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int q = 0; q < w; ++q) acc[q] = add2(acc[q], acc[q + w]);
+  const uint64_t s2 = acc[0];
   float s0, s1;
   unpack2(s2, s0, s1);
   return s0 + s1;
