@@ -842,16 +842,17 @@ struct GParams {
   int* status;
 };
 
-// Source and destination of gathered row w (src null: zero row).
-__device__ __forceinline__ void gather_row(const GParams& P, int64_t w, int64_t rows_q, const uint4*& src,
-                                           uint4*& dst) {
+// Source and destination of gathered row w (src null: zero row).  Index
+// arithmetic in type I (32-bit whenever the row count allows).
+template <class I>
+__device__ __forceinline__ void gather_row(const GParams& P, I w, I rows_q, const uint4*& src, uint4*& dst) {
   src = nullptr;
   if (w < rows_q) {
-    const int64_t per = static_cast<int64_t>(P.Hkv) * P.Rpad;
+    const I per = static_cast<I>(P.Hkv) * P.Rpad;
     const int ai = static_cast<int>(w / per);
-    const int64_t rem = w - ai * per;
+    const I rem = w - static_cast<I>(ai) * per;
     const int h = static_cast<int>(rem / P.Rpad);
-    const int R = static_cast<int>(rem - static_cast<int64_t>(h) * P.Rpad);
+    const int R = static_cast<int>(rem - static_cast<I>(h) * P.Rpad);
     const int layer = P.layer[ai];
     const int nc = P.n_chunks[ai];
     const int r = min(R / P.CR, nc - 1);
@@ -869,12 +870,12 @@ __device__ __forceinline__ void gather_row(const GParams& P, int64_t w, int64_t 
         record_status(P.status, DEV_BOUNDS);
     }
   } else {
-    const int64_t w2 = w - rows_q;
-    const int64_t per = static_cast<int64_t>(P.Hkv) * P.Q;
+    const I w2 = w - rows_q;
+    const I per = static_cast<I>(P.Hkv) * P.Q;
     const int ai = static_cast<int>(w2 / per);
-    const int64_t rem = w2 - ai * per;
+    const I rem = w2 - static_cast<I>(ai) * per;
     const int h = static_cast<int>(rem / P.Q);
-    const int t = static_cast<int>(rem - static_cast<int64_t>(h) * P.Q);
+    const int t = static_cast<int>(rem - static_cast<I>(h) * P.Q);
     const int layer = P.layer[ai];
     dst = reinterpret_cast<uint4*>(P.Kg + ((static_cast<int64_t>(layer) * P.Hkv + h) * P.Q + t) * kHeadDim);
     const int s = P.sel ? P.sel[t] : t;
@@ -886,20 +887,20 @@ __device__ __forceinline__ void gather_row(const GParams& P, int64_t w, int64_t 
   }
 }
 
+template <class I, int ROWS>
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GParams P) {
-  constexpr int ROWS = 4;
-  const int64_t rows_q = static_cast<int64_t>(P.n_active) * P.Hkv * P.Rpad;
-  const int64_t rows_k = P.Kg ? static_cast<int64_t>(P.n_active) * P.Hkv * P.Q : 0;
-  const int64_t total = rows_q + rows_k;
+  const I rows_q = static_cast<I>(P.n_active) * P.Hkv * P.Rpad;
+  const I rows_k = P.Kg ? static_cast<I>(P.n_active) * P.Hkv * P.Q : 0;
+  const I total = rows_q + rows_k;
   const int sub = threadIdx.x & 15;
-  const int64_t hw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 4);
-  for (int64_t w0 = hw; w0 < total; w0 += stride * ROWS) {
+  const I hw = static_cast<I>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4);
+  const I stride = static_cast<I>(gridDim.x) * (blockDim.x >> 4);
+  for (I w0 = hw; w0 < total; w0 += stride * ROWS) {
     uint4 val[ROWS];
     uint4* dst[ROWS];
 #pragma unroll
     for (int u = 0; u < ROWS; ++u) {
-      const int64_t w = w0 + u * stride;
+      const I w = w0 + u * stride;
       dst[u] = nullptr;
       val[u] = make_uint4(0, 0, 0, 0);
       if (w < total) {
@@ -969,7 +970,13 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
     if (blocks < 1) blocks = 1;
     {
       ProfScope ps("recon_gather", st);
-      gather_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(gp);
+      // 32-bit row arithmetic while every index (plus one grid stride of
+      // look-ahead) stays below 2^31
+      const int64_t slack = blocks * 16 * 4 * 2;
+      if (rows + slack < (int64_t(1) << 31))
+        gather_kernel<int, 4><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
+      else
+        gather_kernel<int64_t, 4><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
