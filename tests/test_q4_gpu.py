@@ -50,7 +50,7 @@ def check_codec(qk, X):
     return codes, params, Y
 
 
-@pytest.mark.parametrize("rows", [1, 2, 3, 17, 1000, 65537])
+@pytest.mark.parametrize("rows", [1, 2, 3, 17, 1000, 65537, 200003])
 def test_random_rows(qk, rows):
     cfg = ks.DecodeConfig("q4", seqs=1, Hkv=1, G=1, kept=rows, seed=rows)
     x = ks.gen_decode(cfg, DEV)
