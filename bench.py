@@ -386,20 +386,33 @@ def run_ours(args, cfg, rank, world, local_rank):
         hK = torch.from_numpy(x.K.view(np.int16)).view(torch.bfloat16).pin_memory()
         hV = torch.from_numpy(x.V.view(np.int16)).view(torch.bfloat16).pin_memory()
         hQ = torch.from_numpy(x.Q.view(np.int16)).view(torch.bfloat16).pin_memory()
-        hkept = torch.empty(kept.shape, dtype=torch.int32).pin_memory()
-        hKc = torch.empty(Kc.shape, dtype=torch.bfloat16).pin_memory()
-        hVc = torch.empty(Vc.shape, dtype=torch.bfloat16).pin_memory()
+        hkept = [torch.empty(kept.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
+        hKc = [torch.empty(Kc.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        hVc = [torch.empty(Vc.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        kept2 = [kept, torch.empty_like(kept)]
+        Kc2 = [Kc, torch.empty_like(Kc)]
+        Vc2 = [Vc, torch.empty_like(Vc)]
 
         # K is copied whole (the proxy and the scoring read all of it) into
-        # one of two device buffers on a copy stream, so the next step's copy
-        # overlaps this step's compute; V and the query pool stay in pinned
-        # host memory, mapped into the device address space, and the gather /
-        # compaction kernels read only the selected query rows and the kept
-        # value rows across the link.  Results come back to pinned host memory.
+        # one of two device buffers on a copy stream; V and the query pool stay
+        # in pinned host memory, mapped into the device address space, and the
+        # gather / compaction kernels read only the selected query rows and the
+        # kept value rows across the link.  The next step's K copy starts once
+        # this step's query gather has been issued (kvc_compress_ex records an
+        # event there), so the two do not share the link and the copy runs
+        # under the scoring passes.  Results go back to pinned host memory on a
+        # third stream from double-buffered outputs.
         Kbuf = [K, torch.empty_like(K)]
         copy_stream = torch.cuda.Stream(device=dev)
+        d2h_stream = torch.cuda.Stream(device=dev)
         ev_copied = [torch.cuda.Event(), torch.cuda.Event()]
         ev_free = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        gather_done = [torch.cuda.Event(), torch.cuda.Event()]
+        for evs in (ev_copied, ev_free, ev_out, gather_done):
+            for ev in evs:
+                ev.record(stream)       # create the events
+        torch.cuda.synchronize()
 
         def e2e_steps(n, start_event=None):
             for i in range(n):
@@ -407,16 +420,24 @@ def run_ours(args, cfg, rank, world, local_rank):
                 with torch.cuda.stream(copy_stream):
                     if i == 0 and start_event is not None:
                         copy_stream.wait_event(start_event)
+                    if i > 0:
+                        copy_stream.wait_event(gather_done[(i - 1) % 2])
                     copy_stream.wait_event(ev_free[bsel])
                     Kbuf[bsel].copy_(hK, non_blocking=True)
                     ev_copied[bsel].record(copy_stream)
                 stream.wait_event(ev_copied[bsel])
-                qk.kvc_compress_ex(shape, args.proxy, Kbuf[bsel], hV, hQ, S, cfg.m, cfg.rho, cfg.passes, kl, kept, Kc, Vc, ws=ws,
-                                stream=stream)
+                stream.wait_event(ev_out[bsel])
+                qk.kvc_compress_ex(shape, args.proxy, Kbuf[bsel], hV, hQ, S, cfg.m, cfg.rho, cfg.passes, kl,
+                                   kept2[bsel], Kc2[bsel], Vc2[bsel], ws=ws, stream=stream,
+                                   gather_done=gather_done[bsel])
                 ev_free[bsel].record(stream)
-                hkept.copy_(kept, non_blocking=True)
-                hKc.copy_(Kc, non_blocking=True)
-                hVc.copy_(Vc, non_blocking=True)
+                with torch.cuda.stream(d2h_stream):
+                    d2h_stream.wait_event(ev_free[bsel])
+                    hkept[bsel].copy_(kept2[bsel], non_blocking=True)
+                    hKc[bsel].copy_(Kc2[bsel], non_blocking=True)
+                    hVc[bsel].copy_(Vc2[bsel], non_blocking=True)
+                    ev_out[bsel].record(d2h_stream)
+            stream.wait_stream(d2h_stream)
 
         e2e_steps(2)
         torch.cuda.synchronize()
@@ -439,12 +460,13 @@ def run_ours(args, cfg, rank, world, local_rank):
         # bytes crossing host -> device per step: K copied, plus the query rows
         # and kept V rows the kernels read from mapped host memory
         h2d = hK.numel() * 2 + cfg.passes * L * Hq * work["Q"] * d * 2 + L * H * k * d * 2
-        d2h = hkept.numel() * 4 + (hKc.numel() + hVc.numel()) * 2
+        d2h = hkept[0].numel() * 4 + (hKc[0].numel() + hVc[0].numel()) * 2
         e2e = {"value": world * N * args.e2e_steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.e2e_steps,
-               "how": "pinned host inputs: K copied each step on a copy stream into one of two device buffers "
-                      "(overlapping the previous step's compute); query rows and kept V rows read in place; "
-                      "kept indices and compacted K/V copied back to pinned host memory"}
+               "how": "pinned host inputs: K copied each step on a copy stream into one of two device buffers, "
+                      "starting after the previous step's query gather (overlapping its scoring passes); query "
+                      "rows and kept V rows read in place; kept indices and compacted K/V copied back to pinned "
+                      "host memory on a third stream"}
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None

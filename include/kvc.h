@@ -59,6 +59,7 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st* kvc_stream; /* identical to cudaStream_t */
+typedef struct CUevent_st* kvc_event;   /* identical to cudaEvent_t */
 
 typedef enum {
   KVC_OK = 0,
@@ -233,11 +234,19 @@ KVC_API kvc_status kvc_compress(kvc_shape shape, const void* K, const void* V, c
                         float* p_opt, int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes,
                         kvc_stream stream);
 
-/* kvc_compress with a selectable stage-1 proxy (kvc_compress uses KeyDiff). */
+/* kvc_compress with a selectable stage-1 proxy (kvc_compress uses KeyDiff)
+ * and an optional event `gather_done` (NULL: none), recorded on `stream`
+ * right after the last pass's gather of the reconstruction queries.  When
+ * Qpool (and V) are page-locked host memory read in place, that gather is
+ * the call's last large read across the host link: a caller streaming the
+ * next cache to the device can make its copy wait on this event so that the
+ * two do not compete for the link.  The event must have been created by the
+ * caller (cudaEventCreate*); the library only records it. */
 KVC_API kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K, const void* V,
                                    const void* Qpool, int32_t sinks, int32_t m, double rho, int32_t passes,
                                    const int32_t* k_per_layer, int32_t* kept, void* Kc, void* Vc, float* p_opt,
-                                   int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes, kvc_stream stream);
+                                   int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes, kvc_stream stream,
+                                   kvc_event gather_done);
 
 /* ------------------------------------------------------------------ EpiCache
  * "[26'ICML] EpiCache", "+α: 레이어별 예산 배분": per-layer budgets from a

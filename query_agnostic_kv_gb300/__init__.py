@@ -80,7 +80,7 @@ _SIGS = {
     "kvc_proxy_score_noalloc": (c_i32, [kvc_shape, c_vp, c_vp, c_vp]),
     "kvc_proxy_score_kind": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "kvc_compress_ex": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_i32,
-                                ctypes.POINTER(c_i32), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+                                ctypes.POINTER(c_i32), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "kvc_decode_workspace_size": (c_sz, [c_i32, c_i32, c_i32]),
     "kvc_decode_attention": (c_i32, [c_i32, c_i32, c_vp, c_vp, c_i64, c_vp, c_vp, c_i32, c_vp, ctypes.c_float, c_vp,
                                      c_vp, c_vp, c_sz, c_vp]),
@@ -273,15 +273,22 @@ def kvc_proxy_score_kind(shape, kind, K, p, s=None, ws=None, stream=None) -> Non
 
 
 def kvc_compress_ex(shape, proxy, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, Kc, Vc, p=None, sel=None,
-                    score=None, ws=None, stream=None) -> None:
-    """kvc_compress with a selectable stage-1 proxy ("keydiff" or "knorm")."""
+                    score=None, ws=None, stream=None, gather_done=None) -> None:
+    """kvc_compress with a selectable stage-1 proxy ("keydiff" or "knorm");
+    `gather_done` (a torch.cuda.Event that has been recorded once, so that it
+    exists) is recorded right after the last query gather."""
     w, wb = _ws(ws)
+    ev = None
+    if gather_done is not None:
+        if not gather_done.cuda_event:
+            raise ValueError("gather_done must be a created event (record it once first)")
+        ev = c_vp(gather_done.cuda_event)
     _check("kvc_compress_ex", lib().kvc_compress_ex(
         _shape(shape), _proxy_kind(proxy), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(V, torch.bfloat16, "V"),
         _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"), sinks, m, float(rho), passes, _i32_array(k_per_layer),
         _dev(kept, torch.int32, "kept"), _dev(Kc, torch.bfloat16, "Kc"), _dev(Vc, torch.bfloat16, "Vc"),
         _dev(p, torch.float32, "p"), _dev(sel, torch.int32, "sel"), _dev(score, torch.float32, "score"), w, wb,
-        _stream(stream)))
+        _stream(stream), ev))
 
 
 def kvc_proxy_score_noalloc(shape, K, p, stream=None) -> None:

@@ -227,7 +227,7 @@ cudaStream_t cs(kvc_stream s) { return reinterpret_cast<cudaStream_t>(s); }
 
 kvc_status run_recon(const kvc_shape& s, const ChunkPlan& plan, int32_t sinks, const void* K, const void* Qpool,
                      const int32_t* sel, const void* Kapp, float* score, float* lse_out, const KV2Workspace& w,
-                     cudaStream_t st) {
+                     cudaStream_t st, cudaEvent_t gather_done = nullptr) {
   ReconProblem pr;
   memset(&pr, 0, sizeof(pr));
   pr.L = s.L;
@@ -258,6 +258,7 @@ kvc_status run_recon(const kvc_shape& s, const ChunkPlan& plan, int32_t sinks, c
   pr.score = score;
   pr.ldS = s.N;
   pr.lse_out = lse_out;
+  pr.gather_done = gather_done;
   return cuda_status(launch_recon(pr, w.rw, st));
 }
 
@@ -496,13 +497,13 @@ kvc_status kvc_compress(kvc_shape shape, const void* K, const void* V, const voi
                         float* p_opt, int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes,
                         kvc_stream stream) {
   return kvc_compress_ex(shape, KVC_PROXY_KEYDIFF, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, Kc, Vc,
-                         p_opt, sel_opt, score_opt, ws, ws_bytes, stream);
+                         p_opt, sel_opt, score_opt, ws, ws_bytes, stream, nullptr);
 }
 
 kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K, const void* V, const void* Qpool,
                            int32_t sinks, int32_t m, double rho, int32_t passes, const int32_t* k_per_layer,
                            int32_t* kept, void* Kc, void* Vc, float* p_opt, int32_t* sel_opt, float* score_opt,
-                           void* ws, size_t ws_bytes, kvc_stream stream) {
+                           void* ws, size_t ws_bytes, kvc_stream stream, kvc_event gather_done) {
   ChunkPlan plan;
   if (proxy != KVC_PROXY_KEYDIFF && proxy != KVC_PROXY_KNORM) return KVC_ERR_INVALID;
   if (!shape_ok(shape) || !K || !Qpool || !kept || !Kc || passes < 1 || (V == nullptr) != (Vc == nullptr) ||
@@ -526,7 +527,8 @@ kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K,
   if (pe != cudaSuccess) return KVC_ERR_CUDA;
   for (int t = 0; t < passes; ++t) {
     if (launch_select(p, shape.N, sinks, plan, rho, sel, st) != cudaSuccess) return KVC_ERR_CUDA;
-    kvc_status r = run_recon(shape, plan, sinks, K, Qpool, sel, nullptr, score, nullptr, w, st);
+    kvc_status r = run_recon(shape, plan, sinks, K, Qpool, sel, nullptr, score, nullptr, w, st,
+                             t + 1 == passes ? reinterpret_cast<cudaEvent_t>(gather_done) : nullptr);
     if (r != KVC_OK) return r;
     if (t + 1 < passes && launch_mean_heads(score, LH, shape.N, shape.N, sinks, p, st) != cudaSuccess)
       return KVC_ERR_CUDA;

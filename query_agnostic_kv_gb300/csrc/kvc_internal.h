@@ -149,6 +149,7 @@ struct ReconProblem {
   float* score;       // score + (layer*Hkv + h) * ldS + position
   int64_t ldS;
   float* lse_out;     // optional [L][Hq][Q], natural log
+  cudaEvent_t gather_done;  // optional: recorded right after the query gather is launched
 };
 struct ReconWorkspace {
   void* Qg;       // bf16 [L*Hkv][Rpad][d]

@@ -980,6 +980,10 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (pr.gather_done) {
+      e = cudaEventRecord(pr.gather_done, st);
+      if (e != cudaSuccess) return e;
+    }
   }
 
   // ---- tensor maps

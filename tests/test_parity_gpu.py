@@ -396,3 +396,32 @@ def test_full_size_llama16k_sampled(qk):
     # properties that hold for every head at any size
     assert np.all(np.isfinite(out["score"])) and np.all(out["score"] > 0) and np.all(out["score"] <= 1.0 + 1e-6)
     assert np.all(np.diff(out["kept"], axis=2) > 0)
+
+
+def test_compress_gather_done_event(qk):
+    """The optional gather-done event is recorded and changes nothing."""
+    cfg = ks.scaled(ks.TINY, L=2, Hkv=2, Hq=4, N=1024, m=256)
+    x = ks.gen_kv2(cfg)
+    L, H, Hq, N, S = cfg.L, cfg.Hkv, cfg.Hq, cfg.N, cfg.sinks
+    shape = (L, H, Hq, 128, N)
+    K, V, Q = to_dev(x.K), to_dev(x.V), to_dev(x.Q)
+    k = qk.kvc_budget_count(cfg.budget, N, S)
+    ws = torch.empty(qk.kvc_workspace_size(shape, S, cfg.m, cfg.rho), dtype=torch.uint8, device=DEV)
+    outs = []
+    ev = torch.cuda.Event()
+    ev.record()
+    torch.cuda.synchronize()
+    for use in (False, True):
+        kept = torch.empty(L * H * k, dtype=torch.int32, device=DEV)
+        Kc = torch.empty(L * H * k * 128, dtype=torch.bfloat16, device=DEV)
+        Vc = torch.empty_like(Kc)
+        qk.kvc_compress_ex(shape, "keydiff", K, V, Q, S, cfg.m, cfg.rho, 2, [k] * L, kept, Kc, Vc, ws=ws,
+                           gather_done=ev if use else None)
+        torch.cuda.synchronize()
+        assert qk.kvc_stream_status() == 0
+        outs.append((kept.clone(), Kc.clone(), Vc.clone()))
+    assert ev.query()
+    assert all(torch.equal(a, b) for a, b in zip(*outs))
+    with pytest.raises(ValueError):
+        qk.kvc_compress_ex(shape, "keydiff", K, V, Q, S, cfg.m, cfg.rho, 1, [k] * L, kept, Kc, Vc, ws=ws,
+                           gather_done=torch.cuda.Event())
