@@ -94,9 +94,9 @@ def algorithmic_work(cfg):
 
 # DRAM bytes per launch of the row-LSE kernel as ncu counted them on the
 # 4-layer case of the 16K workload (dram__bytes_read + dram__bytes_write =
-# 202.27 + 4.10 MB); the traffic grows with the number of (layer, KV head)
+# 202.33 + 0.48 MB); the traffic grows with the number of (layer, KV head)
 # pairs.  Reset to None whenever the kernel changes until it is captured again.
-LSE_TRAFFIC_PER_LAYER = (202.27e6 + 4.10e6) / 4
+LSE_TRAFFIC_PER_LAYER = (202.33e6 + 0.48e6) / 4
 
 
 def load_peaks():
