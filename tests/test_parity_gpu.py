@@ -425,3 +425,34 @@ def test_compress_gather_done_event(qk):
     with pytest.raises(ValueError):
         qk.kvc_compress_ex(shape, "keydiff", K, V, Q, S, cfg.m, cfg.rho, 1, [k] * L, kept, Kc, Vc, ws=ws,
                            gather_done=torch.cuda.Event())
+
+
+def test_compress_in_cuda_graph(qk):
+    """After one eager call the whole compression step can be captured into a
+    CUDA graph; replays give the eager results bit for bit."""
+    cfg = ks.scaled(ks.TINY, L=2, Hkv=2, Hq=4, N=1024, m=256)
+    x = ks.gen_kv2(cfg)
+    L, H, Hq, N, S = cfg.L, cfg.Hkv, cfg.Hq, cfg.N, cfg.sinks
+    shape = (L, H, Hq, 128, N)
+    K, V, Q = to_dev(x.K), to_dev(x.V), to_dev(x.Q)
+    k = qk.kvc_budget_count(cfg.budget, N, S)
+    ws = torch.empty(qk.kvc_workspace_size(shape, S, cfg.m, cfg.rho), dtype=torch.uint8, device=DEV)
+    kept = torch.empty(L * H * k, dtype=torch.int32, device=DEV)
+    Kc = torch.empty(L * H * k * 128, dtype=torch.bfloat16, device=DEV)
+    Vc = torch.empty_like(Kc)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        qk.kvc_compress(shape, K, V, Q, S, cfg.m, cfg.rho, 1, [k] * L, kept, Kc, Vc, ws=ws, stream=s)
+    torch.cuda.synchronize()
+    ref = (kept.clone(), Kc.clone(), Vc.clone())
+    kept.zero_(); Kc.zero_(); Vc.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        qk.kvc_compress(shape, K, V, Q, S, cfg.m, cfg.rho, 1, [k] * L, kept, Kc, Vc, ws=ws,
+                        stream=torch.cuda.current_stream())
+    for _ in range(2):
+        kept.zero_(); Kc.zero_(); Vc.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert qk.kvc_stream_status() == 0
+        assert torch.equal(kept, ref[0]) and torch.equal(Kc, ref[1]) and torch.equal(Vc, ref[2])
