@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 
 #include "kvc_internal.h"
+#include "kvc_ptx.cuh"
 
 namespace kvc {
 namespace {
@@ -72,31 +73,47 @@ __device__ __forceinline__ void encode_group(const uint4 w, uint32_t& packed, ui
   const float rs = fast ? __frcp_rn(s) : 0.f;
   // rint(t) for 0 <= t < 2^22: RN(t + 2^23) holds it, ties to even, in its
   // low mantissa bits (a >= 0 because the offset is at most the minimum).
+  // Both values of a 32-bit word are processed as one packed f32x2 pair
+  // (IEEE round-to-nearest like the scalar operations); t - rint(t) is one
+  // fused a*b+c with b = -1 (exact negation, one rounding).  a <= 15 s up to
+  // one rounding, so t < 15.5 and rint(t) <= 15: the low 4 bits are the code.
   constexpr float kMagic = 8388608.f;                  // 2^23
-  float a[8], m[8];
+  const uint64_t nlo2 = pack2(-lo, -lo), rs2 = pack2(rs, rs);
+  const uint64_t mg2 = pack2(kMagic, kMagic), nmg2 = pack2(-kMagic, -kMagic), m1 = pack2(-1.f, -1.f);
+  uint64_t a2[4], m2[4];
   bool near = false;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float x = (k & 1) ? bf16_hi(ww[k >> 1]) : bf16_lo(ww[k >> 1]);
-    a[k] = __fsub_rn(x, lo);
-    const float t = __fmul_rn(a[k], rs);
-    m[k] = __fadd_rn(t, kMagic);
-    near |= fabsf(__fsub_rn(t, __fsub_rn(m[k], kMagic))) > 0.4999f;
+  for (int k = 0; k < 4; ++k) {
+    a2[k] = add2(pack2(bf16_lo(ww[k]), bf16_hi(ww[k])), nlo2);
+    const uint64_t t2 = mul2(a2[k], rs2);
+    m2[k] = add2(t2, mg2);
+    const uint64_t d2 = fma2(add2(m2[k], nmg2), m1, t2);   // t - rint(t)
+    float d0, d1;
+    unpack2(d2, d0, d1);
+    near |= (fabsf(d0) > 0.4999f) | (fabsf(d1) > 0.4999f);
   }
   near = (near || !fast) && s > 0.f;
   if (__any_sync(0xffffffffu, near)) {                 // rare: resolve near-ties with the IEEE quotient
     if (near) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float t = __fmul_rn(a[k], rs);
-        if (!fast || fabsf(__fsub_rn(t, __fsub_rn(m[k], kMagic))) > 0.4999f)
-          m[k] = __fadd_rn(__fdiv_rn(a[k], s), kMagic);
+      for (int k = 0; k < 4; ++k) {
+        float a0, a1, mm0, mm1;
+        unpack2(a2[k], a0, a1);
+        unpack2(m2[k], mm0, mm1);
+        const float t0 = __fmul_rn(a0, rs), t1 = __fmul_rn(a1, rs);
+        if (!fast || fabsf(__fsub_rn(t0, __fsub_rn(mm0, kMagic))) > 0.4999f) mm0 = __fadd_rn(__fdiv_rn(a0, s), kMagic);
+        if (!fast || fabsf(__fsub_rn(t1, __fsub_rn(mm1, kMagic))) > 0.4999f) mm1 = __fadd_rn(__fdiv_rn(a1, s), kMagic);
+        m2[k] = pack2(mm0, mm1);
       }
     }
   }
   packed = 0;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) packed |= min(__float_as_uint(m[k]) & 0x1fu, 15u) << (4 * k);
+  for (int k = 0; k < 4; ++k) {
+    float mm0, mm1;
+    unpack2(m2[k], mm0, mm1);
+    packed |= ((__float_as_uint(mm0) & 0xfu) | ((__float_as_uint(mm1) & 0xfu) << 4)) << (8 * k);
+  }
   param = static_cast<uint32_t>(__bfloat16_as_ushort(s_h)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo_h)) << 16);
 }
 
