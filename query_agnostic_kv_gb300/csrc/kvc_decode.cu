@@ -47,6 +47,9 @@ constexpr int HDR_BYTES = 128;
 #ifndef KVC_DEC_NW
 #define KVC_DEC_NW 15
 #endif
+#ifndef KVC_DEC_NB
+#define KVC_DEC_NB 4
+#endif
 #ifndef KVC_DEC_STAGES
 #define KVC_DEC_STAGES 3
 #endif
@@ -54,7 +57,7 @@ constexpr int HDR_BYTES = 128;
 template <int GP>
 struct DCfg {
   static constexpr int NW = GP <= 4 ? KVC_DEC_NW : 8;        // consumer warps
-  static constexpr int NB = GP <= 4 ? 4 : 2;                 // batches per warp per tile
+  static constexpr int NB = GP <= 4 ? KVC_DEC_NB : 2;        // batches per warp per tile
   static constexpr int STAGES = GP <= 4 ? KVC_DEC_STAGES : 6;
   static constexpr int TK = KPW * NW * NB;                   // keys per stage
   static constexpr int TILE_BYTES = TK * ROW_BYTES;  // one of K or V
