@@ -161,6 +161,43 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Memory kind of `p` as the runtime sees it (cudaMemoryTypeUnregistered for
+// ordinary host memory or an unknown address).
+cudaMemoryType memory_type(const void* p, const void** device_view = nullptr) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return cudaMemoryTypeUnregistered;
+  }
+  if (device_view) *device_view = a.devicePointer;
+  return a.type;
+}
+
+// Device or managed memory (what the tensor-map and device-only inputs need).
+bool is_device_memory(const void* p) {
+  const cudaMemoryType t = memory_type(p);
+  return t == cudaMemoryTypeDevice || t == cudaMemoryTypeManaged;
+}
+
+// Whether the current device's kernels may read `p` in place: device or
+// managed memory, page-locked host memory mapped at the same address, or
+// ordinary host memory when the device reads pageable memory through the
+// host's page tables (cudaDevAttrPageableMemoryAccess).  Anything else would
+// make a kernel touch an unmapped address, so the call is refused instead.
+bool device_can_read(const void* p) {
+  const void* view = nullptr;
+  const cudaMemoryType t = memory_type(p, &view);
+  if (t == cudaMemoryTypeDevice || t == cudaMemoryTypeManaged) return true;
+  if (t == cudaMemoryTypeHost) return view == p;
+  int d = 0, pageable = 0;
+  if (cudaGetDevice(&d) != cudaSuccess ||
+      cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, d) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return pageable != 0;
+}
+
 kvc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
 
 bool shape_ok(const kvc_shape& s) {
@@ -454,6 +491,7 @@ kvc_status kvc_recon_score(kvc_shape shape, const void* K, const void* Qpool, co
                            size_t ws_bytes, kvc_stream stream) {
   ChunkPlan plan;
   if (!shape_ok(shape) || !K || !Qpool || !sel || !score || !aligned16(K) || !aligned16(Qpool) ||
+      !is_device_memory(K) || !device_can_read(Qpool) ||
       (Kapp_opt && !aligned16(Kapp_opt)) || !make_plan(shape.N, sinks, m, rho, &plan))
     return KVC_ERR_INVALID;
   KV2Workspace w = carve_kv2(shape, plan, ws, ws_bytes);
@@ -486,6 +524,7 @@ kvc_status kvc_compact(kvc_shape shape, const void* K, const void* V, const int3
   if (!shape_ok(shape) || !K || !kept || !Kc || (V == nullptr) != (Vc == nullptr) || !aligned16(K) ||
       !aligned16(Kc) || (V && (!aligned16(V) || !aligned16(Vc))))
     return KVC_ERR_INVALID;
+  if (!device_can_read(K) || (V && !device_can_read(V))) return KVC_ERR_INVALID;
   if (check_budgets(shape, 0, k_per_layer) != KVC_OK) return KVC_ERR_INVALID;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
@@ -510,6 +549,7 @@ kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K,
       !aligned16(K) || !aligned16(Qpool) || !aligned16(Kc) || (V && (!aligned16(V) || !aligned16(Vc))) ||
       !make_plan(shape.N, sinks, m, rho, &plan))
     return KVC_ERR_INVALID;
+  if (!is_device_memory(K) || !device_can_read(Qpool) || (V && !device_can_read(V))) return KVC_ERR_INVALID;
   if (check_budgets(shape, sinks, k_per_layer) != KVC_OK) return KVC_ERR_INVALID;
   KV2Workspace w = carve_kv2(shape, plan, ws, ws_bytes);
   kvc_status e = check_ws(ws, ws_bytes, w.bytes);
@@ -871,15 +911,6 @@ bool is_pinned_host(const void* p) {
   return a.type == cudaMemoryTypeHost;
 }
 
-bool is_device_mem(const void* p) {
-  cudaPointerAttributes a{};
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
-}
-
 }  // namespace
 
 extern "C" {
@@ -926,9 +957,9 @@ kvc_status kvc_episode_pack(const kvc_block_state* st, void* Kp, void* Vp, int32
 
 kvc_status kvc_episode_swap(const void* dev_out, void* host_out, size_t bytes_out, const void* host_in, void* dev_in,
                             size_t bytes_in, kvc_stream out_stream, kvc_stream in_stream) {
-  if (bytes_out > 0 && (!dev_out || !host_out || !is_device_mem(dev_out) || !is_pinned_host(host_out)))
+  if (bytes_out > 0 && (!dev_out || !host_out || !is_device_memory(dev_out) || !is_pinned_host(host_out)))
     return KVC_ERR_INVALID;
-  if (bytes_in > 0 && (!host_in || !dev_in || !is_pinned_host(host_in) || !is_device_mem(dev_in)))
+  if (bytes_in > 0 && (!host_in || !dev_in || !is_pinned_host(host_in) || !is_device_memory(dev_in)))
     return KVC_ERR_INVALID;
   if (bytes_out > 0) {
     cudaError_t e = cudaMemcpyAsync(host_out, dev_out, bytes_out, cudaMemcpyDeviceToHost, cs(out_stream));
@@ -963,6 +994,7 @@ kvc_status kvc_q4_decode(int64_t rows, const void* codes, const void* params, vo
   if (!X || !codes || !params || !aligned16(X) || (reinterpret_cast<uintptr_t>(codes) & 3u) ||
       (reinterpret_cast<uintptr_t>(params) & 3u))
     return KVC_ERR_INVALID;
+  if (!device_can_read(codes) || !device_can_read(params)) return KVC_ERR_INVALID;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
   return cuda_status(launch_q4_decode(rows, codes, params, X, cs(stream)));

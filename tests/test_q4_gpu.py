@@ -101,3 +101,44 @@ def test_round_trip_feeds_decode_attention(qk):
     assert qk.kvc_stream_status() == 0
     rel = ((outs[0] - outs[1]).norm() / outs[0].norm()).item()
     assert rel < 0.25, rel
+
+
+def test_decode_refuses_or_reads_pageable_memory(qk):
+    """Ordinary (pageable) host memory is either refused on the host before any
+    launch, or -- when the device reads pageable memory through the host's
+    page tables -- decoded correctly; it never reaches a kernel otherwise."""
+    import ctypes
+    cfg = ks.DecodeConfig("q4p", seqs=1, Hkv=1, G=1, kept=777, seed=5)
+    X = ks.gen_decode(cfg, DEV)["K"]
+    codes, params = encode_gpu(qk, X)
+    hc, hp = codes.cpu(), params.cpu()            # pageable copies
+    assert not hc.is_pinned()
+    Y = torch.zeros_like(X)
+    rc = qk.lib().kvc_q4_decode(X.shape[0], ctypes.c_void_p(hc.data_ptr()), ctypes.c_void_p(hp.data_ptr()),
+                                ctypes.c_void_p(Y.data_ptr()), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc in (0, 1)
+    torch.cuda.synchronize()
+    assert qk.kvc_stream_status() == 0
+    if rc == 0:
+        Y2 = torch.empty_like(X)
+        qk.kvc_q4_decode(codes, params, Y2)
+        assert torch.equal(Y, Y2)
+    else:
+        assert torch.count_nonzero(Y) == 0
+
+
+def test_compress_refuses_host_keys(qk):
+    import ctypes
+    x = ks.gen_kv2(ks.scaled(ks.TINY, N=512, m=128))
+    K = torch.from_numpy(x.K.view(np.int16)).view(torch.bfloat16)          # host, pageable
+    Q = torch.from_numpy(x.Q.view(np.int16)).view(torch.bfloat16).to(DEV)
+    shape = qk.shape_of(1, 1, 4, 512)
+    kept = torch.empty(64, dtype=torch.int32, device=DEV)
+    Kc = torch.empty(64 * 128, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(qk.kvc_workspace_size(shape, 4, 128, 0.1), dtype=torch.uint8, device=DEV)
+    k = (ctypes.c_int32 * 1)(25)
+    rc = qk.lib().kvc_compress(shape, ctypes.c_void_p(K.data_ptr()), None, ctypes.c_void_p(Q.data_ptr()), 4, 128,
+                               0.1, 1, k, ctypes.c_void_p(kept.data_ptr()), ctypes.c_void_p(Kc.data_ptr()), None,
+                               None, None, None, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 1
