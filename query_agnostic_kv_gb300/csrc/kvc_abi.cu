@@ -160,6 +160,9 @@ using namespace kvc;
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+namespace kvc {
 
 // Memory kind of `p` as the runtime sees it (cudaMemoryTypeUnregistered for
 // ordinary host memory or an unknown address).
@@ -198,7 +201,21 @@ bool device_can_read(const void* p) {
   return pageable != 0;
 }
 
+}  // namespace kvc
+
+namespace {
+
+
 kvc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
+
+// Every non-null pointer argument a kernel will dereference must be memory the
+// device can reach (see device_can_read); otherwise the call is refused before
+// any launch.
+bool reachable() { return true; }
+template <class T, class... R>
+bool reachable(const T* p, const R*... rest) {
+  return (p == nullptr || device_can_read(p)) && reachable(rest...);
+}
 
 bool shape_ok(const kvc_shape& s) {
   if (s.L < 1 || s.L > kMaxLayers || s.Hkv < 1 || s.Hq < s.Hkv || s.Hq % s.Hkv != 0 || s.d != kHeadDim || s.N < 1)
@@ -463,6 +480,7 @@ kvc_status kvc_proxy_score_kind(kvc_shape shape, kvc_proxy_kind kind, const void
                                 void* ws, size_t ws_bytes, kvc_stream stream) {
   if (!shape_ok(shape) || !K || !p || !aligned16(K) || (kind != KVC_PROXY_KEYDIFF && kind != KVC_PROXY_KNORM))
     return KVC_ERR_INVALID;
+  if (!reachable(K, p, s_opt, ws)) return KVC_ERR_INVALID;
   float* s = s_opt;
   if (!s) {
     // per-head scratch lives in the score region of the workspace
@@ -480,7 +498,7 @@ kvc_status kvc_proxy_score_kind(kvc_shape shape, kvc_proxy_kind kind, const void
 kvc_status kvc_select_queries(int32_t N, int32_t sinks, int32_t m, double rho, const float* p, int32_t* sel,
                               kvc_stream stream) {
   ChunkPlan plan;
-  if (!p || !sel || !make_plan(N, sinks, m, rho, &plan)) return KVC_ERR_INVALID;
+  if (!p || !sel || !make_plan(N, sinks, m, rho, &plan) || !reachable(p, sel)) return KVC_ERR_INVALID;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
   return cuda_status(launch_select(p, N, sinks, plan, rho, sel, cs(stream)));
@@ -492,7 +510,8 @@ kvc_status kvc_recon_score(kvc_shape shape, const void* K, const void* Qpool, co
   ChunkPlan plan;
   if (!shape_ok(shape) || !K || !Qpool || !sel || !score || !aligned16(K) || !aligned16(Qpool) ||
       !is_device_memory(K) || !device_can_read(Qpool) ||
-      (Kapp_opt && !aligned16(Kapp_opt)) || !make_plan(shape.N, sinks, m, rho, &plan))
+      (Kapp_opt && !aligned16(Kapp_opt)) || !make_plan(shape.N, sinks, m, rho, &plan) ||
+      !reachable(sel, score, lse_opt, Kapp_opt, ws))
     return KVC_ERR_INVALID;
   KV2Workspace w = carve_kv2(shape, plan, ws, ws_bytes);
   kvc_status e = check_ws(ws, ws_bytes, w.bytes);
@@ -503,7 +522,8 @@ kvc_status kvc_recon_score(kvc_shape shape, const void* K, const void* Qpool, co
 }
 
 kvc_status kvc_refine_proxy(kvc_shape shape, const float* score, int32_t sinks, float* p, kvc_stream stream) {
-  if (!shape_ok(shape) || !score || !p || sinks < 0 || sinks >= shape.N) return KVC_ERR_INVALID;
+  if (!shape_ok(shape) || !score || !p || sinks < 0 || sinks >= shape.N || !reachable(score, p))
+    return KVC_ERR_INVALID;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
   return cuda_status(launch_mean_heads(score, shape.L * shape.Hkv, shape.N, shape.N, sinks, p, cs(stream)));
@@ -511,7 +531,8 @@ kvc_status kvc_refine_proxy(kvc_shape shape, const float* score, int32_t sinks, 
 
 kvc_status kvc_evict_topk(kvc_shape shape, float* score, int32_t sinks, const int32_t* k_per_layer, int32_t* kept,
                           void* ws, size_t ws_bytes, kvc_stream stream) {
-  if (!shape_ok(shape) || !score || !kept || sinks < 0 || sinks >= shape.N) return KVC_ERR_INVALID;
+  if (!shape_ok(shape) || !score || !kept || sinks < 0 || sinks >= shape.N || !reachable(score, kept, ws))
+    return KVC_ERR_INVALID;
   if (check_budgets(shape, sinks, k_per_layer) != KVC_OK) return KVC_ERR_INVALID;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < 256) return KVC_ERR_WORKSPACE;
   kvc_status d = device_ok();
@@ -524,7 +545,7 @@ kvc_status kvc_compact(kvc_shape shape, const void* K, const void* V, const int3
   if (!shape_ok(shape) || !K || !kept || !Kc || (V == nullptr) != (Vc == nullptr) || !aligned16(K) ||
       !aligned16(Kc) || (V && (!aligned16(V) || !aligned16(Vc))))
     return KVC_ERR_INVALID;
-  if (!device_can_read(K) || (V && !device_can_read(V))) return KVC_ERR_INVALID;
+  if (!device_can_read(K) || (V && !device_can_read(V)) || !reachable(kept, Kc, Vc)) return KVC_ERR_INVALID;
   if (check_budgets(shape, 0, k_per_layer) != KVC_OK) return KVC_ERR_INVALID;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
@@ -549,7 +570,9 @@ kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K,
       !aligned16(K) || !aligned16(Qpool) || !aligned16(Kc) || (V && (!aligned16(V) || !aligned16(Vc))) ||
       !make_plan(shape.N, sinks, m, rho, &plan))
     return KVC_ERR_INVALID;
-  if (!is_device_memory(K) || !device_can_read(Qpool) || (V && !device_can_read(V))) return KVC_ERR_INVALID;
+  if (!is_device_memory(K) || !device_can_read(Qpool) || (V && !device_can_read(V)) ||
+      !reachable(kept, Kc, Vc, p_opt, sel_opt, score_opt, ws))
+    return KVC_ERR_INVALID;
   if (check_budgets(shape, sinks, k_per_layer) != KVC_OK) return KVC_ERR_INVALID;
   KV2Workspace w = carve_kv2(shape, plan, ws, ws_bytes);
   kvc_status e = check_ws(ws, ws_bytes, w.bytes);
@@ -620,6 +643,8 @@ kvc_status kvc_block_state_init(kvc_block_state* st, int32_t L, int32_t Hkv, int
       sinks < 0 || capacity < 1 || !K0 || !V0 || !pos0 || !K1 || !V1 || !pos1 || !aligned16(K0) ||
       !aligned16(V0) || !aligned16(K1) || !aligned16(V1))
     return KVC_ERR_INVALID;
+  // key slabs are tensor-map sources; the rest is read and written in place
+  if (!is_device_memory(K0) || !is_device_memory(K1) || !reachable(V0, V1, pos0, pos1)) return KVC_ERR_INVALID;
   if (static_cast<int64_t>(L) * Hq * capacity >= (int64_t(1) << 31)) return KVC_ERR_INVALID;
   for (int l = 0; l < L; ++l)
     if (budgets[l] < sinks || budgets[l] > capacity) return KVC_ERR_INVALID;
@@ -686,6 +711,7 @@ kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk, const v
   if (!st || !Kblk || !Vblk || !Qprompt || !Kprompt || blk_len < 1 || P < 1 || !aligned16(Kblk) ||
       !aligned16(Vblk) || !aligned16(Qprompt) || !aligned16(Kprompt))
     return KVC_ERR_INVALID;
+  if (!reachable(Kblk, Vblk, Qprompt, Kprompt, ws)) return KVC_ERR_INVALID;
   if (st->consumed + blk_len > INT32_MAX) return KVC_ERR_INVALID;
   for (int l = 0; l < st->L; ++l)
     if (st->len[l] + static_cast<int64_t>(blk_len) > st->capacity) return KVC_ERR_INVALID;
@@ -850,6 +876,10 @@ kvc_status kvc_decode_attention(int32_t n_seg, int32_t G, const void* Kc, const 
   if (!Kc || !Vc || !seg_off || !seg_len || !q || !out || !aligned16(Kc) || !aligned16(Vc) || !aligned16(q) ||
       (reinterpret_cast<uintptr_t>(out) & 3u) != 0 || (lse_opt && (reinterpret_cast<uintptr_t>(lse_opt) & 3u)))
     return KVC_ERR_INVALID;
+  // K, V and q are bulk-copy sources; the rest is read or written in place
+  if (!is_device_memory(Kc) || !is_device_memory(Vc) || !is_device_memory(q) ||
+      !reachable(seg_off, seg_len, out, lse_opt, ws))
+    return KVC_ERR_INVALID;
   if (int64_t(n_seg) * G * kHeadDim >= (int64_t(1) << 31)) return KVC_ERR_INVALID;
   const DecodePlan pl = make_decode_plan(n_seg, G, max_len);
   if (int64_t(n_seg) * pl.n_split >= (int64_t(1) << 31)) return KVC_ERR_INVALID;
@@ -922,6 +952,7 @@ kvc_status kvc_episode_match(int32_t B, int32_t E, int32_t De, const float* quer
   if (!queries || !centroids || !episode || !aligned16(queries) || !aligned16(centroids) ||
       (reinterpret_cast<uintptr_t>(episode) & 3u) || (dist2_opt && (reinterpret_cast<uintptr_t>(dist2_opt) & 3u)))
     return KVC_ERR_INVALID;
+  if (!reachable(queries, centroids, episode, dist2_opt)) return KVC_ERR_INVALID;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
   return cuda_status(launch_match(B, E, De, queries, centroids, tau, episode, dist2_opt, cs(stream)));
@@ -937,6 +968,7 @@ int64_t kvc_episode_rows(const kvc_block_state* st) {
 kvc_status kvc_episode_pack(const kvc_block_state* st, void* Kp, void* Vp, int32_t* pos_opt, kvc_stream stream) {
   if (kvc_episode_rows(st) < 0 || !Kp || !Vp || !aligned16(Kp) || !aligned16(Vp) || st->d != kHeadDim)
     return KVC_ERR_INVALID;
+  if (!reachable(Kp, Vp, pos_opt)) return KVC_ERR_INVALID;
   PackParams pp{};
   pp.L = st->L;
   pp.Hkv = st->Hkv;
@@ -983,6 +1015,7 @@ kvc_status kvc_q4_encode(int64_t rows, const void* X, void* codes, void* params,
   if (!X || !codes || !params || !aligned16(X) || (reinterpret_cast<uintptr_t>(codes) & 3u) ||
       (reinterpret_cast<uintptr_t>(params) & 3u))
     return KVC_ERR_INVALID;
+  if (!reachable(X, codes, params)) return KVC_ERR_INVALID;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
   return cuda_status(launch_q4_encode(rows, X, codes, params, cs(stream)));
@@ -994,7 +1027,7 @@ kvc_status kvc_q4_decode(int64_t rows, const void* codes, const void* params, vo
   if (!X || !codes || !params || !aligned16(X) || (reinterpret_cast<uintptr_t>(codes) & 3u) ||
       (reinterpret_cast<uintptr_t>(params) & 3u))
     return KVC_ERR_INVALID;
-  if (!device_can_read(codes) || !device_can_read(params)) return KVC_ERR_INVALID;
+  if (!device_can_read(codes) || !device_can_read(params) || !reachable(X)) return KVC_ERR_INVALID;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
   return cuda_status(launch_q4_decode(rows, codes, params, X, cs(stream)));

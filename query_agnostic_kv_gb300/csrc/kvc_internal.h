@@ -13,6 +13,14 @@ namespace kvc {
 constexpr int kHeadDim = 128;
 constexpr int kMaxLayers = KVC_MAX_LAYERS;
 
+// Memory checks made on the host before a launch.  is_device_memory: device
+// or managed memory (tensor-map and bulk-copy sources).  device_can_read:
+// memory kernels may read or write in place -- device or managed memory,
+// page-locked host memory mapped at the same address, or pageable host memory
+// on a device that reaches it through the host page tables.
+bool is_device_memory(const void* p);
+bool device_can_read(const void* p);
+
 // Per-device status word (device address) and the process-wide wait limit.
 int* status_word();
 uint64_t wait_limit_ns();

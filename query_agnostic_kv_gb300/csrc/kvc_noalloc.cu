@@ -37,6 +37,7 @@ extern "C" kvc_status kvc_proxy_score_noalloc(kvc_shape shape, const void* K, fl
   if (shape.L < 1 || shape.Hkv < 1 || shape.Hq < shape.Hkv || shape.Hq % shape.Hkv != 0 || shape.d != kHeadDim ||
       shape.N < 1 || !K || !p || (reinterpret_cast<uintptr_t>(K) & 15u) != 0)
     return KVC_ERR_INVALID;
+  if (!device_can_read(K) || !device_can_read(p)) return KVC_ERR_INVALID;
   const size_t need = static_cast<size_t>(shape.L) * shape.Hkv * shape.N;
   if (need > kScratchFloats) return KVC_ERR_WORKSPACE;  // larger than the built-in scratch
   const kvc_status dc = kvc_device_check();
