@@ -8,7 +8,10 @@
 // every CTA adds them in rank order (so the result is deterministic and the
 // same in every CTA), then each CTA re-reads its slice -- the first rows
 // from a shared-memory copy kept during pass A, the rest from L2 -- and
-// writes s (pass B).  A second small kernel averages s over the heads.
+// writes s (pass B).  Pass A also stores 1/|k_i| in s[i]; pass B reads it
+// back on the same lane (the row -> lane mapping is the same in both passes),
+// so it forms only k_i . U before overwriting s[i] with the score.  A second
+// small kernel averages s over the heads.
 //
 // Each 256-byte key row is handled by half a warp: lane l16 owns channels
 // [8*l16, 8*l16 + 8) as one 16-byte load.
@@ -47,26 +50,60 @@ constexpr int CACHE_ROWS = KVC_KD_CACHE;  // rows of the slice kept in shared me
 constexpr bool PASS_B_REVERSE = KVC_KD_REVERSE != 0;
 constexpr int SMEM_BYTES = CACHE_ROWS * 256 + HALVES * 128 * 4;
 
-__device__ __forceinline__ void unpack8(const uint4& q, float (&f)[8]) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&q);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __bfloat1622float2(b[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
+// ---------------------------------------------------------------------------
+// Per-row arithmetic of the KeyDiff kernel.  Channel products run on packed
+// f32x2 pairs, and the eight rows a half-warp has in flight are reduced
+// together: a transposing butterfly leaves row u's total on lanes 2u and
+// 2u+1 of the half-warp after 15 shuffles for all eight rows (a butterfly per
+// row takes 32).
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
-
-__device__ __forceinline__ float half_warp_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 8);
-  v += __shfl_xor_sync(0xffffffffu, v, 4);
-  v += __shfl_xor_sync(0xffffffffu, v, 2);
-  v += __shfl_xor_sync(0xffffffffu, v, 1);
-  return v;
+// The same pair built with byte permutes.  Pass A unpacks each row twice
+// (for |k|^2, then for the unit-key sum once 1/|k| is known); spelling the
+// second unpack differently keeps the compiler from holding all 64 unpacked
+// values of the eight rows live across the reduction.
+__device__ __forceinline__ uint64_t bf2_to_f2_prmt(uint32_t w) {
+  return pack2(__uint_as_float(__byte_perm(w, 0u, 0x1044)), __uint_as_float(__byte_perm(w, 0u, 0x3244)));
+}
+__device__ __forceinline__ float sumsq8(const uint4& q) {
+  const uint64_t x0 = bf2_to_f2(q.x), x1 = bf2_to_f2(q.y), x2 = bf2_to_f2(q.z), x3 = bf2_to_f2(q.w);
+  uint64_t a = mul2(x0, x0);
+  a = fma2(x1, x1, a);
+  a = fma2(x2, x2, a);
+  a = fma2(x3, x3, a);
+  float lo, hi;
+  unpack2(a, lo, hi);
+  return lo + hi;
+}
+__device__ __forceinline__ float dot8(const uint4& q, const uint64_t (&u2)[4]) {
+  uint64_t a = mul2(bf2_to_f2(q.x), u2[0]);
+  a = fma2(bf2_to_f2(q.y), u2[1], a);
+  a = fma2(bf2_to_f2(q.z), u2[2], a);
+  a = fma2(bf2_to_f2(q.w), u2[3], a);
+  float lo, hi;
+  unpack2(a, lo, hi);
+  return lo + hi;
+}
+// v[u] holds this lane's partial for row u (u = 0..7) of its half-warp.
+// Returns the half-warp total of row (l16 >> 1), present on lanes 2u, 2u+1.
+__device__ __forceinline__ float transpose_sum8(const float (&v)[8], int l16) {
+  const bool b3 = (l16 & 8) != 0, b2 = (l16 & 4) != 0, b1 = (l16 & 2) != 0;
+  float r[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)   // keep rows k + 4*b3
+    r[k] = (b3 ? v[k + 4] : v[k]) + __shfl_xor_sync(0xffffffffu, b3 ? v[k] : v[k + 4], 8);
+  float r2[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k)   // keep rows k + 2*b2 + 4*b3
+    r2[k] = (b2 ? r[k + 2] : r[k]) + __shfl_xor_sync(0xffffffffu, b2 ? r[k] : r[k + 2], 4);
+  const float r3 = (b1 ? r2[1] : r2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? r2[0] : r2[1], 2);
+  return r3 + __shfl_xor_sync(0xffffffffu, r3, 1);
 }
 
 __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_PER_SM)
     keydiff_kernel(const __nv_bfloat16* __restrict__ K, int N, float* __restrict__ s_out) {
+  static_assert(UNROLL == 8, "rows are reduced in groups of eight");
   extern __shared__ __align__(16) uint8_t smem[];
   uint4* cache = reinterpret_cast<uint4*>(smem);                            // [CACHE_ROWS][16]
   float* red = reinterpret_cast<float*>(smem + CACHE_ROWS * 256);          // [HALVES][128]
@@ -78,17 +115,19 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
   const int rank = static_cast<int>(cluster.block_rank());
   const int lh = blockIdx.y;
   const uint4* rows = reinterpret_cast<const uint4*>(K + static_cast<int64_t>(lh) * N * kHeadDim);
+  float* srow = s_out + static_cast<int64_t>(lh) * N;
 
   const int slice = (N + CLUSTER - 1) / CLUSTER;
   const int i0 = min(rank * slice, N);
   const int i1 = min(i0 + slice, N);
+  const int lane = threadIdx.x & 31;
   const int hw = threadIdx.x >> 4;
   const int l16 = threadIdx.x & 15;
+  const int u_own = l16 >> 1;                 // row (of the eight) this lane ends up owning
+  const bool writer = (l16 & 1) == 0;
 
-  // ---- pass A: sum of unit keys over the slice
-  float acc[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+  // ---- pass A: sum of unit keys over the slice; 1/|k_i| kept in s[i]
+  uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
   for (int base = i0; base < i1; base += HALVES * UNROLL) {
     uint4 q[UNROLL];
 #pragma unroll
@@ -96,23 +135,34 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
       const int i = base + u * HALVES + hw;
       q[u] = (i < i1) ? __ldg(rows + static_cast<int64_t>(i) * 16 + l16) : make_uint4(0, 0, 0, 0);
     }
+    float ss[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int i = base + u * HALVES + hw;
       if (i < i1 && i - i0 < CACHE_ROWS) cache[(i - i0) * 16 + l16] = q[u];
-      float f[8];
-      unpack8(q[u], f);
-      float ss = 0.f;
+      ss[u] = sumsq8(q[u]);
+    }
+    const float tot = transpose_sum8(ss, l16);
+    const float inv_own = tot > 0.f ? rsqrtf(tot) : 0.f;
+    const int i_own = base + u_own * HALVES + hw;
+    if (writer && i_own < i1) srow[i_own] = inv_own;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) ss = fmaf(f[c], f[c], ss);
-      ss = half_warp_sum(ss);
-      const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = fmaf(f[c], inv, acc[c]);
+    for (int u = 0; u < UNROLL; ++u) {
+      const float iv = __shfl_sync(0xffffffffu, inv_own, (lane & 16) | (u << 1));
+      const uint64_t iv2 = pack2(iv, iv);
+      acc2[0] = fma2(bf2_to_f2_prmt(q[u].x), iv2, acc2[0]);
+      acc2[1] = fma2(bf2_to_f2_prmt(q[u].y), iv2, acc2[1]);
+      acc2[2] = fma2(bf2_to_f2_prmt(q[u].z), iv2, acc2[2]);
+      acc2[3] = fma2(bf2_to_f2_prmt(q[u].w), iv2, acc2[3]);
     }
   }
 #pragma unroll
-  for (int c = 0; c < 8; ++c) red[hw * 128 + l16 * 8 + c] = acc[c];
+  for (int c = 0; c < 4; ++c) {
+    float a, b;
+    unpack2(acc2[c], a, b);
+    red[hw * 128 + l16 * 8 + 2 * c] = a;
+    red[hw * 128 + l16 * 8 + 2 * c + 1] = b;
+  }
   __syncthreads();
   if (threadIdx.x < kHeadDim) {
     float t = 0.f;
@@ -136,14 +186,16 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
   __syncthreads();
 
   // ---- pass B: s_i = -(k_i . U) / (|k_i| |U|)
-  float uu[8];
+  uint64_t u2[4];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) uu[c] = U[l16 * 8 + c];
+  for (int c = 0; c < 4; ++c) u2[c] = pack2(U[l16 * 8 + 2 * c], U[l16 * 8 + 2 * c + 1]);
   const float uinv = unorm_inv;
-  float* srow = s_out + static_cast<int64_t>(lh) * N;
   const int nblk = (i1 - i0 + HALVES * UNROLL - 1) / (HALVES * UNROLL);
   for (int bi = 0; bi < nblk; ++bi) {
     const int base = i0 + (PASS_B_REVERSE ? nblk - 1 - bi : bi) * HALVES * UNROLL;
+    const int i_own = base + u_own * HALVES + hw;
+    // 1/|k| of the owned row, written by this same lane in pass A
+    const float inv_own = (writer && i_own < i1) ? srow[i_own] : 0.f;
     uint4 q[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
@@ -153,51 +205,41 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
       else
         q[u] = make_uint4(0, 0, 0, 0);
     }
+    float dt[UNROLL];
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const int i = base + u * HALVES + hw;
-      float f[8];
-      unpack8(q[u], f);
-      float ss = 0.f, dot = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        ss = fmaf(f[c], f[c], ss);
-        dot = fmaf(f[c], uu[c], dot);
-      }
-      ss = half_warp_sum(ss);
-      dot = half_warp_sum(dot);
-      if (l16 == 0 && i < i1) srow[i] = (ss > 0.f && uinv > 0.f) ? -dot * rsqrtf(ss) * uinv : 0.f;
-    }
+    for (int u = 0; u < UNROLL; ++u) dt[u] = dot8(q[u], u2);
+    const float dot = transpose_sum8(dt, l16);
+    if (writer && i_own < i1) srow[i_own] = (inv_own > 0.f && uinv > 0.f) ? -dot * inv_own * uinv : 0.f;
   }
 }
 
 // Knorm proxy (KV² page, "전제와 한계": the close alternative to KeyDiff):
 // s_i = -|k_i| per (layer, KV head), one read of K.  Half a warp per 256-byte
-// row, eight rows in flight per half-warp.
+// row, eight rows in flight per half-warp, reduced together as in KeyDiff.
+// The loop runs on the warp's even half-warp index so that both halves of a
+// warp take the same trips through the shuffles; rows are guarded one by one.
 __global__ void __launch_bounds__(256) knorm_kernel(const uint4* __restrict__ K, int64_t rows,
                                                     float* __restrict__ s_out) {
   constexpr int R = 8;
   const int l16 = threadIdx.x & 15;
   const int64_t hw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 4);
-  for (int64_t r0 = hw; r0 < rows; r0 += stride * R) {
+  const int64_t hw_even = hw & ~int64_t(1);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 4);   // even
+  const int u_own = l16 >> 1;
+  for (int64_t b = hw_even; b < rows; b += stride * R) {
+    const int64_t r0 = b + (hw - hw_even);
     uint4 q[R];
 #pragma unroll
     for (int u = 0; u < R; ++u) {
       const int64_t r = r0 + u * stride;
       q[u] = (r < rows) ? __ldg(K + r * 16 + l16) : make_uint4(0, 0, 0, 0);
     }
+    float ss[R];
 #pragma unroll
-    for (int u = 0; u < R; ++u) {
-      float f[8];
-      unpack8(q[u], f);
-      float ss = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) ss = fmaf(f[c], f[c], ss);
-      ss = half_warp_sum(ss);
-      const int64_t r = r0 + u * stride;
-      if (l16 == 0 && r < rows) s_out[r] = -sqrtf(ss);
-    }
+    for (int u = 0; u < R; ++u) ss[u] = sumsq8(q[u]);
+    const float tot = transpose_sum8(ss, l16);
+    const int64_t r = r0 + u_own * stride;
+    if ((l16 & 1) == 0 && r < rows) s_out[r] = -sqrtf(tot);
   }
 }
 

@@ -19,9 +19,11 @@
 //                       while single-buffered accumulators are handed back to
 //                       the MMA warp as soon as they are read.
 //   pass 2 (column max) A = 2 tiles of 128 cache keys of one chunk, B = the
-//                       chunk's query rows, double-buffered accumulators.
-//                       Each consumer thread owns one key (TMEM lane) and
-//                       folds max_j (x_ij - lse2_j) over every query column;
+//                       chunk's query rows in 256-row tiles, one accumulator
+//                       per key tile read by two consumer groups (128 query
+//                       columns each).  Each consumer thread owns one key
+//                       (TMEM lane) and folds max_j (x_ij - lse2_j) over its
+//                       query columns;
 //                       exp2 is monotone, so one exp2 per key gives the max
 //                       attention.  One store per position.
 //
@@ -74,16 +76,20 @@ struct Cfg<1> {
   static constexpr bool A_TMEM = false; // A read by the MMA from shared memory
 };
 // Pass 2: two 128-key A tiles per unit against 256-query B tiles (MMA
-// N = 256), one consumer group per accumulator reading its 256 columns in four
-// 64-column loads (the accumulator is released after the fourth).  Measured
-// against 128-query tiles with the key tiles in TMEM (A_TMEM, still
-// selectable) and against two 128-column consumer groups per accumulator
-// (CSPLIT = 2, whose end-of-unit merge path remains): this shape was fastest.
+// N = 256), two consumer groups per accumulator, each reading its 128 query
+// columns in four 32-column loads (the accumulator is released after the
+// fourth) and merging the two halves of a key's maximum at the end of the
+// unit.  The accumulators are single-buffered, so the time a group holds one
+// is on the MMA's critical path: halving it measured 6% faster than one
+// group of four 64-column loads.  Also measured and slower: 128-query tiles
+// with the key tiles in TMEM (A_TMEM, still selectable), loads of the next
+// column block issued before folding the current one, and the last query
+// tile of a chunk multiplied at its own (smaller) N.
 #ifndef KVC_P2_BN
 #define KVC_P2_BN 256
 #endif
 #ifndef KVC_P2_CSPLIT
-#define KVC_P2_CSPLIT 1
+#define KVC_P2_CSPLIT 2
 #endif
 #ifndef KVC_P2_KST
 #define KVC_P2_KST 2
@@ -102,6 +108,27 @@ struct Cfg<2> {
   static constexpr bool A_TMEM = KVC_P2_ATMEM != 0;
 };
 constexpr uint32_t TMEM_A_BASE = 256;  // pass 2: A buffers at TMEM columns [256, 512), 64 columns per tile
+// Pass 2 refills its single A buffer (the next unit's 128-key tiles, read
+// once from HBM) only after the unit's last MMA; the producer warms those
+// tiles in L2 once the unit's second B tile is on its way.
+#ifndef KVC_A_PREFETCH
+#define KVC_A_PREFETCH 1
+#endif
+constexpr bool A_PREFETCH = KVC_A_PREFETCH != 0;
+// Pass-2 consumer columns per TMEM load: 32 lets two consumer groups share
+// each accumulator within the register file (64 fits one group).
+#ifndef KVC_P2_BLK
+#define KVC_P2_BLK 32
+#endif
+constexpr int P2_BLK = KVC_P2_BLK;
+static_assert(P2_BLK == 32 || P2_BLK == 64, "pass-2 TMEM load width");
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[W]) {
+  if constexpr (W == 32)
+    tmem_ld32(taddr, v);
+  else
+    tmem_ld64(taddr, v);
+}
 template <int PASS>
 constexpr int kThreads = 64 + 128 * Cfg<PASS>::NA * Cfg<PASS>::CSPLIT;
 template <int PASS>
@@ -513,26 +540,37 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
       uint32_t bph = 0, aph = 0;
       int issued_b[MAX_KST] = {};
       int issued_a[2] = {0, 0};
+      // A tile t of a unit (128 rows; pass 2 reads them through the 128-row K maps)
+      auto a_tile = [&](const Unit& W, int t, int32_t& y) -> const CUtensorMap* {
+        if (PASS == 1) {
+          y = W.lh * P.Rpad + W.R0 + t * TILE_ROWS;
+          return &tmQg;
+        }
+        y = static_cast<int32_t>(W.lh * P.ldK + W.key0 + t * TILE_ROWS);
+        return W.slab ? &tmK1 : &tmK0;
+      };
       for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
         const Unit U = decode_unit<PASS>(P, u);
-        // A tiles (128 rows each; pass 2 reads them through the 128-row K maps)
         if (!mbar_wait(&bars->a_empty[ab], aph ^ 1, P.limit_ns)) { fail(); break; }
         mbar_arrive_expect_tx(&bars->a_full[ab], U.ntile * TILE_BYTES);
         for (int t = 0; t < U.ntile; ++t) {
           uint8_t* dst = sA + (ab * NA + t) * TILE_BYTES;
-          const CUtensorMap* map;
           int32_t y;
-          if (PASS == 1) {
-            map = &tmQg;
-            y = U.lh * P.Rpad + U.R0 + t * TILE_ROWS;
-          } else {
-            map = U.slab ? &tmK1 : &tmK0;
-            y = static_cast<int32_t>(U.lh * P.ldK + U.key0 + t * TILE_ROWS);
-          }
+          const CUtensorMap* map = a_tile(U, t, y);
           tma_load_2d(dst, map, 0, y, &bars->a_full[ab]);
           tma_load_2d(dst + AHALF, map, 64, y, &bars->a_full[ab]);
         }
         issued_a[ab]++;
+        auto prefetch_next = [&]() {
+          if (u + static_cast<int>(gridDim.x) >= P.n_units) return;
+          const Unit W = decode_unit<PASS>(P, u + gridDim.x);
+          for (int t = 0; t < W.ntile; ++t) {
+            int32_t y;
+            const CUtensorMap* map = a_tile(W, t, y);
+            tma_prefetch_l2_2d(map, 0, y);
+            tma_prefetch_l2_2d(map, 64, y);
+          }
+        };
         if (++ab == ABUF) { ab = 0; aph ^= 1; }
         // B tiles (BN rows each)
         for (int i = 0; i < U.nT; ++i) {
@@ -559,6 +597,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
           tma_load_2d(dst + BHALF, map, 64, y, &bars->b_full[s]);
           issued_b[s]++;
+          if (PASS == 2 && A_PREFETCH && i == min(1, U.nT - 1)) prefetch_next();
           if (++s == KST) { s = 0; bph ^= 1; }
         }
       }
@@ -735,7 +774,8 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         // ---- column max over the chunk's queries: one key (TMEM lane) per
         // thread, this group's half of the accumulator's query columns
         constexpr int COLS = BN / CSPLIT;
-        static_assert(COLS % 64 == 0, "pass-2 consumers read whole 64-column blocks");
+        constexpr int PB = P2_BLK;                       // columns per TMEM load
+        static_assert(COLS % PB == 0, "pass-2 consumers read whole column blocks");
         const int pos = U.key0 + wg * TILE_ROWS + row;
         const bool valid = has_tile && pos < U.hi;
         const int rows_q = P.G * nq_of(P, U.ai, U.r);    // query rows of this chunk
@@ -755,26 +795,16 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           float t[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) t[q] = -INFINITY;
+          // fold one block of query columns into t (bl: valid columns of the block)
+          auto fold = [&](auto& v, int blk, int bl) {
+            constexpr int W = sizeof(v) / sizeof(float);   // columns of the block
+            if (bl < W) {
 #pragma unroll
-          for (int blk = 0; blk < COLS / 64; ++blk) {
-            float v[64];
-            __syncwarp();
-            tmem_ld64(col + blk * 64, v);
-            if (blk == COLS / 64 - 1) {
-              // the accumulator goes back to the MMA warp once it is in registers
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
+              for (int k = 0; k < W; ++k) v[k] = (k < bl) ? v[k] : -INFINITY;
             }
-            const int bl = lim - blk * 64;
-            if (bl <= 0) continue;
-            if (bl < 64) {
+            const float4* l4 = reinterpret_cast<const float4*>(lrow + blk * W);
 #pragma unroll
-              for (int k = 0; k < 64; ++k) v[k] = (k < bl) ? v[k] : -INFINITY;
-            }
-            const float4* l4 = reinterpret_cast<const float4*>(lrow + blk * 64);
-#pragma unroll
-            for (int k4 = 0; k4 < 16; ++k4) {
+            for (int k4 = 0; k4 < W / 4; ++k4) {
               const float4 l = l4[k4];
               float x0, x1, x2, x3;
               unpack2(fma2(pack2(v[4 * k4], v[4 * k4 + 1]), cc, pack2(-l.x, -l.y)), x0, x1);
@@ -782,6 +812,20 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
               t[(2 * k4) & 7] = fmax3(t[(2 * k4) & 7], x0, x1);
               t[(2 * k4 + 1) & 7] = fmax3(t[(2 * k4 + 1) & 7], x2, x3);
             }
+          };
+#pragma unroll
+          for (int blk = 0; blk < COLS / PB; ++blk) {
+            float v[PB];
+            __syncwarp();
+            tmem_ld_cols(col + blk * PB, v);
+            if (blk == COLS / PB - 1) {
+              // the accumulator goes back to the MMA warp once it is in registers
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
+            }
+            const int bl = lim - blk * PB;
+            if (bl > 0) fold(v, blk, bl);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->b_empty[cs]);
