@@ -170,6 +170,37 @@ def test_compress_matches_stages_and_is_deterministic(qk):
     assert np.array_equal(res[0][0].reshape(L, H, k), stages["kept"])
 
 
+def test_proxies_past_knorm_grid_cap(qk):
+    """Both proxies on one head whose row count passes the Knorm kernel's
+    grid cap (8 blocks of 128 rows per SM) by one row: there the first
+    half-warp of the first warp takes one more trip through its loop than its
+    partner.  Zero keys are planted (their score is 0 under both proxies)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N = sms * 8 * 128 + 1
+    rng = np.random.default_rng(7)
+    z = rng.standard_normal((1, 1, N, 128), dtype=np.float32)
+    z[..., ::32] += 5.0
+    z *= np.exp(0.3 * rng.standard_normal((1, 1, N, 1))).astype(np.float32)
+    z[0, 0, [0, 5, N - 1]] = 0.0
+    bits = ks.f32_to_bf16_bits(z)
+    K = to_dev(bits)
+    shape = (1, 1, 4, 128, N)
+    ws = torch.empty(qk.kvc_workspace_size(shape, 4, 4096, 0.1), dtype=torch.uint8, device=DEV)
+    p = torch.empty(N, dtype=torch.float32, device=DEV)
+    s = torch.empty(N, dtype=torch.float32, device=DEV)
+    for kind, floor in (("knorm", 0.0), ("keydiff", compare.PROXY_FLOOR)):
+        s.fill_(float("nan"))
+        qk.kvc_proxy_score_kind(shape, kind, K, p, s, ws=ws)
+        assert qk.kvc_stream_status() == 0
+        p_ref, s_ref = kv2.proxy_scores(bits, kind=kind)
+        got = s.cpu().numpy().reshape(1, 1, N)
+        compare.assert_scores(got, s_ref, rtol=1e-5 if kind == "knorm" else compare.SCORE_RTOL, floor=floor,
+                              what=f"{kind} s")
+        compare.assert_scores(p.cpu().numpy(), p_ref, rtol=1e-5 if kind == "knorm" else compare.SCORE_RTOL,
+                              floor=floor, what=f"{kind} p")
+        assert np.all(got[0, 0, [0, 5, N - 1]] == 0.0)
+
+
 @pytest.mark.parametrize("name", ["tiny-4k", "ragged-1000"])
 def test_knorm_proxy_and_pipeline(qk, name):
     """Knorm proxy (s = -|k|, mean over heads) against the oracle, and the
