@@ -108,19 +108,35 @@ int num_sms() {
   return g_sms[d];
 }
 
+namespace {
+bool encode_fn_ready() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+}  // namespace
+
+bool make_tmap_rows16(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  if (!encode_fn_ready()) return false;
+  if (rows == 0) rows = 1;
+  cuuint64_t dims[2] = {16, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {32};
+  cuuint32_t box[2] = {16, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
+  if (!encode_fn_ready()) return false;
   if (rows == 0) rows = 1;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
@@ -266,7 +282,7 @@ KV2Workspace carve_kv2(const kvc_shape& s, const ChunkPlan& plan, void* base, si
   w.rw.Rpad = recon_rows(G, plan.n_chunks, plan.nq_full, plan.nq_last);
   w.rw.Qg = c.take<uint16_t>(LH * w.rw.Rpad * kHeadDim);
   w.rw.Kg = c.take<uint16_t>(LH * plan.Q * kHeadDim);
-  w.rw.lse2 = c.take<float>(LH * w.rw.Rpad + 256);   // + tail read by 256-row pass-2 lse copies
+  w.rw.lsx = c.take<uint16_t>(LH * w.rw.Rpad * 16);
   w.bytes = ((c.used + 255) & ~size_t(255)) + 256;
   w.ok = c.ok;
   return w;
@@ -689,7 +705,7 @@ BlockWorkspace carve_block(const kvc_block_state* st, int32_t P, void* base, siz
   w.rw.Rpad = recon_rows(G, 1, P, P);
   w.rw.Qg = c.take<uint16_t>(LH * w.rw.Rpad * kHeadDim);
   w.rw.Kg = nullptr;
-  w.rw.lse2 = c.take<float>(LH * w.rw.Rpad + 256);   // + tail read by 256-row pass-2 lse copies
+  w.rw.lsx = c.take<uint16_t>(LH * w.rw.Rpad * 16);
   w.bytes = ((c.used + 255) & ~size_t(255)) + 256;
   w.ok = c.ok;
   return w;

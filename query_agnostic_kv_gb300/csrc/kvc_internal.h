@@ -72,6 +72,8 @@ struct Carver {
 // 2-D bf16 tensor map over `rows` rows of 128 elements, box = 64 x box_rows,
 // 128-byte swizzle (the K-major tcgen05 operand layout).
 bool make_tmap_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
+// Rows of 16 bf16 (32 B) in boxes of box_rows rows, 32-byte swizzle.
+bool make_tmap_rows16(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
 
 // ------------------------------------------------------------------ launchers
 // Each returns cudaSuccess or the launch error.
@@ -162,12 +164,11 @@ struct ReconProblem {
 struct ReconWorkspace {
   void* Qg;       // bf16 [L*Hkv][Rpad][d]
   void* Kg;       // bf16 [L*Hkv][Q][d] (gathered appended keys), when Kapp is null
-  float* lse2;    // f32 [L*Hkv][Rpad] (log2 units)
+  void* lsx;      // bf16 [L*Hkv][Rpad][16]: -lse2/scale (row LSE, log2 units) as three bf16 terms, then zeros
   int32_t Rpad;   // rows per (l, h) in Qg, multiple of 128
 };
 // Rows per (layer, KV head) of the query row space (chunks padded to 128 rows).
 int32_t recon_rows(int G, int n_chunks, int nq_full, int nq_last);
-size_t recon_ws_bytes(int L, int Hkv, int G, int n_chunks, int nq_full, int nq_last, int Q, bool need_kg);
 cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaStream_t st);
 
 // Device-side wait that expires on purpose (status-path test).

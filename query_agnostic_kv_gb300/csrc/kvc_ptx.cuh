@@ -122,6 +122,18 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for a K-major operand 16 bf16 (32 B) wide stored with the 32-byte
+// swizzle: 8-row atoms of 256 B stacked every 256 B (one K = 16 step).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused: K fits the swizzle width)
+  d |= static_cast<uint64_t>(256 >> 4) << 32;           // stride byte offset: 8 rows * 32 B
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(6) << 61;                  // swizzle mode: 32 B
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                 // D format: f32
@@ -234,25 +246,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
-}
-
-// ---------------------------------------------------------------- A operand in TMEM
-// Copy one 128-row x 16-element (256-bit) K slice of a K-major operand from
-// shared memory (described like an MMA operand) into 8 TMEM columns: row r
-// goes to lane r, two bf16 per 32-bit column.  Asynchronous, ordered with the
-// issuing thread's later tcgen05.mma.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 }  // namespace kvc

@@ -17,15 +17,16 @@
 //                       MMA logit rate at d = 128, so 16 consumer warps (4
 //                       per SM sub-partition) keep the exponentials flowing
 //                       while single-buffered accumulators are handed back to
-//                       the MMA warp as soon as they are read.
+//                       the MMA warp as soon as they are read.  Each row's
+//                       -lse2/scale is written as three bf16 terms.
 //   pass 2 (column max) A = 2 tiles of 128 cache keys of one chunk, B = the
-//                       chunk's query rows in 256-row tiles, one accumulator
-//                       per key tile read by two consumer groups (128 query
-//                       columns each).  Each consumer thread owns one key
-//                       (TMEM lane) and folds max_j (x_ij - lse2_j) over its
-//                       query columns;
-//                       exp2 is monotone, so one exp2 per key gives the max
-//                       attention.  One store per position.
+//                       chunk's query rows in 256-row tiles.  A ninth K step
+//                       multiplies a constant block of ones with the query
+//                       rows' -lse2/scale terms, so each accumulator already
+//                       holds x_ij - lse2_j/scale; each consumer thread owns
+//                       one key (TMEM lane) and takes the max over the query
+//                       columns.  exp2 is monotone, so one exp2 per key gives
+//                       the max attention.  One store per position.
 //
 // Query rows are laid out per (layer, KV head) in a "row space": chunk r
 // occupies rows [r*CR, r*CR + G*nq_r) ordered (query head g, query j), with
@@ -46,7 +47,6 @@ constexpr int TILE_ROWS = 128;                  // rows of an A tile (TMEM lanes
 constexpr int TILE_BYTES = TILE_ROWS * 256;     // 128 rows x 128 bf16
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_KST = 4;
-constexpr int LSE_PAD = 256;                    // lse2 tail padding (floats): pass-2 bulk copies of a last tile
 
 // Per-pass shape of the pipeline.  B tiles of 256 rows (MMA N = 256) halve
 // the A-operand re-reads from shared memory per FLOP; with N = 128 the
@@ -73,29 +73,26 @@ struct Cfg<1> {
   static constexpr int BN = KVC_P1_BN;  // rows (keys) of a B tile = MMA N
   static constexpr int CSPLIT = KVC_P1_CSPLIT;  // consumer warps sharing one TMEM lane quarter (column split)
   static constexpr int KST = KVC_P1_KST;  // B-tile ring depth
-  static constexpr bool A_TMEM = false; // A read by the MMA from shared memory
 };
 // Pass 2: two 128-key A tiles per unit against 256-query B tiles (MMA
-// N = 256), two consumer groups per accumulator, each reading its 128 query
-// columns in four 32-column loads (the accumulator is released after the
-// fourth) and merging the two halves of a key's maximum at the end of the
-// unit.  The accumulators are single-buffered, so the time a group holds one
-// is on the MMA's critical path: halving it measured 6% faster than one
-// group of four 64-column loads.  Also measured and slower: 128-query tiles
-// with the key tiles in TMEM (A_TMEM, still selectable), loads of the next
+// N = 256, nine K steps: eight of d = 128, one for the lse), one consumer
+// group per accumulator reading its 256 columns in four 64-column loads (the
+// accumulator is released after the fourth).  With the lse subtraction inside
+// the MMA this pass is bound by the tensor pipe (8 layers of the 16K
+// workload: 0.295 ms, against 0.347 ms when the consumers subtracted a staged
+// lse row, and the same 0.295 ms with two 128-column consumer groups per
+// accumulator).  Also measured, all slower, while the consumers subtracted:
+// 128-query tiles with the key tiles copied into TMEM, loads of the next
 // column block issued before folding the current one, and the last query
 // tile of a chunk multiplied at its own (smaller) N.
 #ifndef KVC_P2_BN
 #define KVC_P2_BN 256
 #endif
 #ifndef KVC_P2_CSPLIT
-#define KVC_P2_CSPLIT 2
+#define KVC_P2_CSPLIT 1
 #endif
 #ifndef KVC_P2_KST
 #define KVC_P2_KST 2
-#endif
-#ifndef KVC_P2_ATMEM
-#define KVC_P2_ATMEM 0
 #endif
 template <>
 struct Cfg<2> {
@@ -105,9 +102,7 @@ struct Cfg<2> {
   static constexpr int BN = KVC_P2_BN;
   static constexpr int CSPLIT = KVC_P2_CSPLIT;
   static constexpr int KST = KVC_P2_KST;
-  static constexpr bool A_TMEM = KVC_P2_ATMEM != 0;
 };
-constexpr uint32_t TMEM_A_BASE = 256;  // pass 2: A buffers at TMEM columns [256, 512), 64 columns per tile
 // Pass 2 refills its single A buffer (the next unit's 128-key tiles, read
 // once from HBM) only after the unit's last MMA; the producer warms those
 // tiles in L2 once the unit's second B tile is on its way.
@@ -115,10 +110,10 @@ constexpr uint32_t TMEM_A_BASE = 256;  // pass 2: A buffers at TMEM columns [256
 #define KVC_A_PREFETCH 1
 #endif
 constexpr bool A_PREFETCH = KVC_A_PREFETCH != 0;
-// Pass-2 consumer columns per TMEM load: 32 lets two consumer groups share
-// each accumulator within the register file (64 fits one group).
+// Pass-2 consumer columns per TMEM load (32 lets two consumer groups share
+// an accumulator within the register file).
 #ifndef KVC_P2_BLK
-#define KVC_P2_BLK 32
+#define KVC_P2_BLK 64
 #endif
 constexpr int P2_BLK = KVC_P2_BLK;
 static_assert(P2_BLK == 32 || P2_BLK == 64, "pass-2 TMEM load width");
@@ -137,17 +132,20 @@ template <int PASS>
 constexpr int kBStage = Cfg<PASS>::BN * 256;
 template <int PASS>
 constexpr int kCombBytes = Cfg<PASS>::CSPLIT > 1 ? Cfg<PASS>::NA * TILE_ROWS * 8 : 0;
+// Pass 2 subtracts each query row's lse inside the MMA: a ninth K = 16 step
+// multiplies a constant keys-side block (ones at K = 0..2) with a
+// queries-side block holding -lse2/scale as three bf16 terms (about 24
+// bits), so the accumulator already holds x_ij - lse2_j/scale and the
+// consumers only take maxima.
 template <int PASS>
-constexpr int kLseStage = PASS == 2 ? Cfg<PASS>::BN * 4 : 0;   // pass 2: lse2 of the B tile's query rows
+constexpr int kBxStage = PASS == 2 ? Cfg<PASS>::BN * 32 : 0;   // the B tile's lse rows, 16 bf16 each
 template <int PASS>
-constexpr int kSmemBytes = 1024 + kABytes<PASS> + Cfg<PASS>::KST * (kBStage<PASS> + kLseStage<PASS>) +
-                           kCombBytes<PASS> + 256;
+constexpr int kAxBytes = PASS == 2 ? TILE_ROWS * 32 : 0;       // the constant keys-side block
+template <int PASS>
+constexpr int kSmemBytes = 1024 + kABytes<PASS> + Cfg<PASS>::KST * (kBStage<PASS> + kBxStage<PASS>) +
+                           kAxBytes<PASS> + kCombBytes<PASS> + 256;
 static_assert(Cfg<1>::NA * Cfg<1>::DBUF * Cfg<1>::BN <= TMEM_COLS, "TMEM pass 1");
-static_assert(Cfg<2>::A_TMEM ? (Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_A_BASE &&
-                                TMEM_A_BASE + 2 * Cfg<2>::NA * 64 <= TMEM_COLS)
-                             : Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_COLS,
-              "TMEM pass 2");
-static_assert(Cfg<2>::BN <= LSE_PAD, "lse2 padding covers a pass-2 tile");
+static_assert(Cfg<2>::NA * Cfg<2>::DBUF * Cfg<2>::BN <= TMEM_COLS, "TMEM pass 2");
 static_assert(kSmemBytes<1> <= 232448 && kSmemBytes<2> <= 232448, "shared memory budget of one CTA");
 static_assert(Cfg<1>::KST <= MAX_KST && Cfg<2>::KST <= MAX_KST, "ring depth");
 
@@ -168,7 +166,7 @@ struct KParams {
   int32_t units1;                     // pass-1 units per (l, h)
   int n_units;
   float scale_log2;                   // log2(e) / sqrt(d)
-  float* lse2;
+  __nv_bfloat16* lsx;                 // [rows][16]: -lse2/scale_log2 in three bf16 terms
   float* lse_out;
   float* score;
   int64_t ldS;
@@ -223,6 +221,25 @@ __device__ __forceinline__ uint64_t exp2_poly2(float x0, float x1) {
   const float r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
   const float r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
   return pack2(r0, r1);
+}
+
+// Row o of the lse rows: x = -lse2/scale as three bf16 terms (hi + mid + lo
+// carries about 24 bits; each remainder is exact in fp32), then 13 zeros.
+// -inf (padding rows) is stored as (-inf, 0, 0).
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+__device__ __forceinline__ void store_lse_row(__nv_bfloat16* lsx, int64_t o, float x) {
+  const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+  __nv_bfloat16 hi = __float2bfloat16_rn(x), mid = zero, lo = zero;
+  if (isfinite(x)) {
+    const float r1 = x - __bfloat162float(hi);
+    mid = __float2bfloat16_rn(r1);
+    lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  }
+  uint4* dst = reinterpret_cast<uint4*>(lsx + o * 16);
+  dst[0] = make_uint4(bf16x2_bits(hi, mid), bf16x2_bits(lo, zero), 0u, 0u);
+  dst[1] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 __device__ __forceinline__ int nq_of(const KParams& P, int ai, int r) {
@@ -347,7 +364,6 @@ struct __align__(8) Bars {
   uint64_t b_full[MAX_KST], b_empty[MAX_KST];
   uint64_t d_full[4], d_empty[4];  // per (accumulator buffer, A tile)
   uint64_t comb_full[2], comb_empty[2];  // pass 1: hand-off of the second column half per A tile
-  uint64_t ta_free[2];                   // pass 2: TMEM A buffer no longer read by the MMAs
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -477,7 +493,6 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
                  const __grid_constant__ KParams P) {
   constexpr int NA = Cfg<PASS>::NA, ABUF = Cfg<PASS>::ABUF, DBUF = Cfg<PASS>::DBUF;
   constexpr int BN = Cfg<PASS>::BN, CSPLIT = Cfg<PASS>::CSPLIT, KST = Cfg<PASS>::KST;
-  constexpr int NCW = 4 * NA * CSPLIT;             // consumer warps
   constexpr int BSTAGE = kBStage<PASS>;            // bytes of one B tile
   constexpr int BHALF = BSTAGE / 2;                // one 64-column swizzled half of a B tile
   constexpr int AHALF = TILE_BYTES / 2;
@@ -485,10 +500,11 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;                              // [ABUF][NA] tiles
   uint8_t* sB = smem + kABytes<PASS>;              // [KST] tiles of BN rows
-  constexpr int LSE_STAGE = kLseStage<PASS>;
-  float* sL = reinterpret_cast<float*>(sB + KST * BSTAGE);                      // [KST][BN] (pass 2)
-  float2* sComb = reinterpret_cast<float2*>(sB + KST * (BSTAGE + LSE_STAGE));  // [NA][128] column-half hand-off
-  Bars* bars = reinterpret_cast<Bars*>(sB + KST * (BSTAGE + LSE_STAGE) + kCombBytes<PASS>);
+  constexpr int BX_STAGE = kBxStage<PASS>;
+  uint8_t* sBx = sB + KST * BSTAGE;                                     // [KST][BN][16] bf16 (pass 2)
+  uint8_t* sAx = sBx + KST * BX_STAGE;                                  // [128][16] bf16 (pass 2)
+  float2* sComb = reinterpret_cast<float2*>(sAx + kAxBytes<PASS>);      // [NA][128] column-half hand-off
+  Bars* bars = reinterpret_cast<Bars*>(reinterpret_cast<uint8_t*>(sComb) + kCombBytes<PASS>);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -502,18 +518,23 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
     }
     for (int i = 0; i < KST; ++i) {
       mbar_init(&bars->b_full[i], 1);
-      // pass 2: a stage also holds the B tile's lse2 row, which the consumer
-      // warps read after the MMA has finished with the tile
-      mbar_init(&bars->b_empty[i], PASS == 2 ? 1 + NCW : 1);
+      mbar_init(&bars->b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->comb_full[i], 4);
       mbar_init(&bars->comb_empty[i], 4);
-      mbar_init(&bars->ta_free[i], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
+  }
+  if (PASS == 2) {
+    // keys-side block of the lse step: ones at K = 0..2, repeated at K = 8..10
+    // so that the 32-byte swizzle (which may exchange a row's two 16-byte
+    // halves) leaves it unchanged; the queries side is zero at K = 3..15
+    uint4* ax = reinterpret_cast<uint4*>(sAx);
+    for (int i = threadIdx.x; i < TILE_ROWS * 2; i += blockDim.x) ax[i] = make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, TMEM_COLS);
@@ -576,7 +597,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         for (int i = 0; i < U.nT; ++i) {
           if (*abort_flag) break;
           if (!mbar_wait(&bars->b_empty[s], bph ^ 1, P.limit_ns)) { fail(); break; }
-          mbar_arrive_expect_tx(&bars->b_full[s], BSTAGE + LSE_STAGE);
+          mbar_arrive_expect_tx(&bars->b_full[s], BSTAGE + BX_STAGE);
           const CUtensorMap* map;
           int32_t y;
           if (PASS == 1) {
@@ -591,7 +612,8 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           } else {
             map = &tmQg;
             y = U.lh * P.Rpad + U.r * P.CR + i * BN;
-            bulk_load(sL + s * BN, P.lse2 + y, LSE_STAGE, &bars->b_full[s]);
+            // pass 2 receives the lse-row map in the appended-key slot
+            tma_load_2d(sBx + s * BX_STAGE, &tmApp, 0, y, &bars->b_full[s]);
           }
           uint8_t* dst = sB + s * BSTAGE;
           tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
@@ -611,31 +633,13 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
-      constexpr bool ATM = Cfg<PASS>::A_TMEM;
       int s = 0, ab = 0, db = 0;
       uint32_t bph = 0, aph = 0, dph = 0;
-      int tb = 0;                          // TMEM A buffer (A_TMEM passes)
-      uint32_t ta_ph[2] = {0u, 0u};
-      int ta_used[2] = {0, 0};
       for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
         const Unit U = decode_unit<PASS>(P, u);
         if (!mbar_wait(&bars->a_full[ab], aph, P.limit_ns)) { fail(); break; }
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA + (ab * NA) * TILE_BYTES);
-        const uint32_t ta0 = tbase + TMEM_A_BASE + tb * NA * 64;
-        if (ATM) {
-          // the MMAs of the unit that last used this TMEM A buffer are done
-          if (ta_used[tb] && !mbar_wait(&bars->ta_free[tb], ta_ph[tb], P.limit_ns)) { fail(); break; }
-          if (ta_used[tb]) ta_ph[tb] ^= 1;
-          for (int t = 0; t < U.ntile; ++t)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              tmem_cp_128x256b(ta0 + t * 64 + 8 * k,
-                               sdesc_kmajor_sw128(a0 + t * TILE_BYTES + (k >> 2) * AHALF + (k & 3) * 32));
-          // the staging buffer is free once the copies have completed
-          mma_commit(&bars->a_empty[ab]);
-          if (++ab == ABUF) { ab = 0; aph ^= 1; }
-        }
         for (int i = 0; i < U.nT; ++i) {
           if (*abort_flag) break;
           if (!mbar_wait(&bars->b_full[s], bph, P.limit_ns)) { fail(); break; }
@@ -652,11 +656,11 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
               for (int k = 0; k < 8; ++k) {
                 const uint32_t ka = (k >> 2) * AHALF + (k & 3) * 32;
                 const uint32_t kb = (k >> 2) * BHALF + (k & 3) * 32;
-                if (ATM)
-                  mma_bf16_ta(d, ta0 + t * 64 + 8 * k, sdesc_kmajor_sw128(b0 + kb), idesc, k > 0 ? 1u : 0u);
-                else
-                  mma_bf16(d, sdesc_kmajor_sw128(at + ka), sdesc_kmajor_sw128(b0 + kb), idesc, k > 0 ? 1u : 0u);
+                mma_bf16(d, sdesc_kmajor_sw128(at + ka), sdesc_kmajor_sw128(b0 + kb), idesc, k > 0 ? 1u : 0u);
               }
+              if (PASS == 2)   // + (-lse2_j / scale) on every key row
+                mma_bf16(d, sdesc_kmajor_sw32(smem_u32(sAx)), sdesc_kmajor_sw32(smem_u32(sBx + s * BX_STAGE)), idesc,
+                         1u);
             }
             // accumulator t of this tile is complete (missing tiles commit nothing new)
             mma_commit(&bars->d_full[db * NA + t]);
@@ -666,14 +670,8 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           if (++s == KST) { s = 0; bph ^= 1; }
           if (++db == DBUF) { db = 0; dph ^= 1; }
         }
-        if (ATM) {
-          mma_commit(&bars->ta_free[tb]);
-          ta_used[tb] = 1;
-          tb ^= 1;
-        } else {
-          mma_commit(&bars->a_empty[ab]);
-          if (++ab == ABUF) { ab = 0; aph ^= 1; }
-        }
+        mma_commit(&bars->a_empty[ab]);
+        if (++ab == ABUF) { ab = 0; aph ^= 1; }
       }
       // All issued MMAs must finish before TMEM is released.
       mma_commit(&bars->drain);
@@ -693,8 +691,6 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
     int db = 0;
     uint32_t dph = 0;
     uint32_t comb_ph = 0;  // pass 1: phase of the per-unit half-row hand-off
-    int cs = 0;            // pass 2: B stage of the next tile (same order as the MMA warp)
-    uint32_t cph = 0;
     for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
       const Unit U = decode_unit<PASS>(P, u);
       const bool has_tile = wg < U.ntile;
@@ -760,14 +756,14 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           const int64_t o = static_cast<int64_t>(U.lh) * P.Rpad + R;
           if (valid) {
             const float l2 = mrun + lg2(ssum);
-            P.lse2[o] = l2;
+            store_lse_row(P.lsx, o, -l2 / c);
             if (P.lse_out) {
               const int hq = U.h * P.G + g;
               P.lse_out[(static_cast<int64_t>(U.layer) * P.Hq + hq) * P.Q + rr * P.nq_full + j] =
                   l2 * 0.69314718055994531f;
             }
           } else {
-            P.lse2[o] = INFINITY;  // padding rows never win the pass-2 max
+            store_lse_row(P.lsx, o, -INFINITY);   // padding rows never win the pass-2 max
           }
         }
       } else {
@@ -779,39 +775,26 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         const int pos = U.key0 + wg * TILE_ROWS + row;
         const bool valid = has_tile && pos < U.hi;
         const int rows_q = P.G * nq_of(P, U.ai, U.r);    // query rows of this chunk
-        float vmax = -INFINITY;
-        const uint64_t cc = pack2(c, c);
+        float vmax = -INFINITY;   // max_j (x_ij - lse2_j / scale) over this group's query columns
         for (int i = 0; i < U.nT; ++i) {
           uint64_t* df = &bars->d_full[db * NA + wg];
           if (!mbar_wait(df, dph, P.limit_ns)) { fail(); break; }
           tc_fence_after();
-          // the tile's lse2 row arrived with the B tile (already complete
-          // when the MMA ran; this acquires it for this warp)
-          if (!mbar_wait(&bars->b_full[cs], cph, P.limit_ns)) { fail(); break; }
           // columns past the chunk's query rows belong to the next chunk
           const int lim = rows_q - i * BN - chalf * COLS;
-          const float* lrow = sL + cs * BN + chalf * COLS;
           const uint32_t col = lane_addr + (db * NA + wg) * BN + chalf * COLS;
           float t[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) t[q] = -INFINITY;
-          // fold one block of query columns into t (bl: valid columns of the block)
-          auto fold = [&](auto& v, int blk, int bl) {
-            constexpr int W = sizeof(v) / sizeof(float);   // columns of the block
-            if (bl < W) {
+          // fold one block of query columns into t (bl: valid columns of the
+          // block); the accumulator already holds x_ij - lse2_j / scale
+          auto fold = [&](float (&v)[PB], int bl) {
+            if (bl < PB) {
 #pragma unroll
-              for (int k = 0; k < W; ++k) v[k] = (k < bl) ? v[k] : -INFINITY;
+              for (int k = 0; k < PB; ++k) v[k] = (k < bl) ? v[k] : -INFINITY;
             }
-            const float4* l4 = reinterpret_cast<const float4*>(lrow + blk * W);
 #pragma unroll
-            for (int k4 = 0; k4 < W / 4; ++k4) {
-              const float4 l = l4[k4];
-              float x0, x1, x2, x3;
-              unpack2(fma2(pack2(v[4 * k4], v[4 * k4 + 1]), cc, pack2(-l.x, -l.y)), x0, x1);
-              unpack2(fma2(pack2(v[4 * k4 + 2], v[4 * k4 + 3]), cc, pack2(-l.z, -l.w)), x2, x3);
-              t[(2 * k4) & 7] = fmax3(t[(2 * k4) & 7], x0, x1);
-              t[(2 * k4 + 1) & 7] = fmax3(t[(2 * k4 + 1) & 7], x2, x3);
-            }
+            for (int k = 0; k < PB / 2; ++k) t[k & 7] = fmax3(t[k & 7], v[2 * k], v[2 * k + 1]);
           };
 #pragma unroll
           for (int blk = 0; blk < COLS / PB; ++blk) {
@@ -825,11 +808,8 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
               if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
             }
             const int bl = lim - blk * PB;
-            if (bl > 0) fold(v, blk, bl);
+            if (bl > 0) fold(v, bl);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->b_empty[cs]);
-          if (++cs == KST) { cs = 0; cph ^= 1; }
           if (++db == DBUF) { db = 0; dph ^= 1; }
           vmax = fmax3(vmax, fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]));
           vmax = fmax3(vmax, t[6], t[7]);
@@ -851,7 +831,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           }
           comb_ph ^= 1;
         }
-        if (chalf == 0 && valid) P.score[static_cast<int64_t>(U.lh) * P.ldS + pos] = ex2(vmax);
+        if (chalf == 0 && valid) P.score[static_cast<int64_t>(U.lh) * P.ldS + pos] = ex2(vmax * c);
       }
     }
   }
@@ -968,16 +948,6 @@ int32_t recon_rows(int G, int n_chunks, int nq_full, int nq_last) {
   return (n_chunks - 1) * CR + round_up(G * nq_last, TILE_ROWS);
 }
 
-size_t recon_ws_bytes(int L, int Hkv, int G, int n_chunks, int nq_full, int nq_last, int Q, bool need_kg) {
-  const int64_t Rpad = recon_rows(G, n_chunks, nq_full, nq_last);
-  size_t b = 0;
-  auto add = [&](size_t bytes) { b = ((b + 255) & ~size_t(255)) + bytes; };
-  add(static_cast<size_t>(L) * Hkv * Rpad * kHeadDim * 2);            // Qg
-  if (need_kg) add(static_cast<size_t>(L) * Hkv * Q * kHeadDim * 2);  // Kg
-  add((static_cast<size_t>(L) * Hkv * Rpad + LSE_PAD) * 4);            // lse2 (+ tail read by pass-2 bulk copies)
-  return b + 256;
-}
-
 cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaStream_t st) {
   const int G = pr.G;
   // chunk layout is the same for every active layer in one call
@@ -1046,6 +1016,8 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   const void* app = pr.Kapp ? pr.Kapp : ws.Kg;
   const int64_t ldApp = pr.Kapp ? pr.ldApp : pr.Q;
   if (!make_tmap_rows(&tmApp, app, LH * ldApp, Cfg<1>::BN)) return cudaErrorInvalidValue;
+  CUtensorMap tmLx;   // pass 2 (fold): the lse rows, in the appended-key slot
+  if (!make_tmap_rows16(&tmLx, ws.lsx, LH * Rpad, Cfg<2>::BN)) return cudaErrorInvalidValue;
 
   KParams kp;
   memset(&kp, 0, sizeof(kp));
@@ -1067,7 +1039,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   kp.ldApp = static_cast<int32_t>(ldApp);
   kp.units1 = (Rpad + Cfg<1>::NA * TILE_ROWS - 1) / (Cfg<1>::NA * TILE_ROWS);
   kp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
-  kp.lse2 = ws.lse2;
+  kp.lsx = static_cast<__nv_bfloat16*>(ws.lsx);
   kp.lse_out = pr.lse_out;
   kp.score = pr.score;
   kp.ldS = pr.ldS;
@@ -1093,7 +1065,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   if (kp.n_units > 0) {
     ProfScope ps("recon_colmax", st);
     recon_kernel<2><<<kp.n_units < sms ? kp.n_units : sms, kThreads<2>, kSmemBytes<2>, st>>>(tmQgB, tmK0a, tmK1a,
-                                                                                            tmApp, kp);
+                                                                                            tmLx, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
