@@ -35,8 +35,11 @@ namespace {
 #ifndef KVC_KD_REVERSE
 #define KVC_KD_REVERSE 1
 #endif
+#ifndef KVC_KD_CLUSTER
+#define KVC_KD_CLUSTER 8
+#endif
 // 8 CTAs per head, two resident per SM (measured faster than 16-CTA clusters).
-constexpr int CLUSTER = 8;
+constexpr int CLUSTER = KVC_KD_CLUSTER;
 constexpr int THREADS = 512;
 constexpr int CTAS_PER_SM = KVC_KD_CTAS;  // two clusters' CTAs share an SM: one loads while the other waits
 constexpr int HALVES = THREADS / 16;      // half-warps per CTA
@@ -277,6 +280,10 @@ __global__ void mean_heads_kernel(const float* __restrict__ x, int LH, int N, in
 cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(keydiff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if (CLUSTER > 8) {
+    e = cudaFuncSetAttribute(keydiff_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(CLUSTER, LH);
   {
     ProfScope ps("keydiff", st);

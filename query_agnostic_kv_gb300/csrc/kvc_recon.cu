@@ -117,6 +117,13 @@ constexpr bool A_PREFETCH = KVC_A_PREFETCH != 0;
 #endif
 constexpr int P2_BLK = KVC_P2_BLK;
 static_assert(P2_BLK == 32 || P2_BLK == 64, "pass-2 TMEM load width");
+// Pass-1 consumer columns per TMEM load (8 layers of the 16K workload: 64
+// columns 1.25 ms; 32 columns 1.39-1.43 ms, though they free registers).
+#ifndef KVC_P1_BLK
+#define KVC_P1_BLK 64
+#endif
+constexpr int P1_BLK = KVC_P1_BLK;
+static_assert(P1_BLK == 32 || P1_BLK == 64, "pass-1 TMEM load width");
 template <int W>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[W]) {
   if constexpr (W == 32)
@@ -706,7 +713,8 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         const int j = valid ? local - g * nq : 0;
         float mrun = -INFINITY, ssum = 0.f;
         constexpr int COLS = BN / CSPLIT;  // columns of the tile this warp reads
-        static_assert(COLS % 64 == 0, "consumers read whole 64-column blocks");
+        constexpr int PB = P1_BLK;         // columns per TMEM load
+        static_assert(COLS % PB == 0, "consumers read whole column blocks");
         for (int i = 0; i < U.nT; ++i) {
           uint64_t* df = &bars->d_full[db * NA + wg];
           if (!mbar_wait(df, dph, P.limit_ns)) { fail(); break; }
@@ -715,19 +723,19 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           const int lim = ((tr.kind == 0) ? U.n - tr.t0 : ((tr.chunk == rr) ? (j - tr.t0 + 1) : 0)) -
                           chalf * COLS;
           const uint32_t col = lane_addr + (db * NA + wg) * BN + chalf * COLS;
-          // 64-column blocks; the accumulator is handed back to the MMA warp
+          // column blocks; the accumulator is handed back to the MMA warp
           // right after the last block is in registers
 #pragma unroll
-          for (int blk = 0; blk < COLS / 64; ++blk) {
-            float v[64];
+          for (int blk = 0; blk < COLS / PB; ++blk) {
+            float v[PB];
             __syncwarp();
-            tmem_ld64(col + blk * 64, v);
-            if (blk == COLS / 64 - 1) {
+            tmem_ld_cols(col + blk * PB, v);
+            if (blk == COLS / PB - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
             }
-            row_update<64>(v, lim - blk * 64, c, mrun, ssum);
+            row_update<PB>(v, lim - blk * PB, c, mrun, ssum);
           }
           if (++db == DBUF) { db = 0; dph ^= 1; }
         }
