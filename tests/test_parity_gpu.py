@@ -8,6 +8,7 @@ Tolerances: scores 1e-3 relative (proxy with a 1e-3 absolute floor), index
 sets exact up to oracle near-ties within 1e-4 of the threshold, compacted rows
 bit-exact.
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -77,7 +78,7 @@ def run_stages(qk, x, cfg, lse=False, Kapp=None):
     return out
 
 
-def check_all(x, cfg, out, pairs=None, lse=False):
+def check_all(x, cfg, out, pairs=None, lse=False, score_floor=0.0):
     L, H, N, S = cfg.L, cfg.Hkv, cfg.N, cfg.sinks
     # proxy
     p_ref, s_ref = kv2.proxy_scores(x.K)
@@ -91,7 +92,8 @@ def check_all(x, cfg, out, pairs=None, lse=False):
     sc_ref, lse_ref = kv2.recon_scores(x.K, x.Q, out["sel"], chunks, pairs=pairs)
     todo = pairs if pairs is not None else [(l, h) for l in range(L) for h in range(H)]
     for (l, h) in todo:
-        compare.assert_scores(out["score_raw"][l, h, S:], sc_ref[l, h, S:], what=f"recon score l={l} h={h}")
+        compare.assert_scores(out["score_raw"][l, h, S:], sc_ref[l, h, S:], floor=score_floor,
+                              what=f"recon score l={l} h={h}")
         if lse:
             G = cfg.G
             for g in range(G):
@@ -131,6 +133,19 @@ def test_stagewise_parity(qk, name):
     x = ks.gen_kv2(cfg)
     out = run_stages(qk, x, cfg, lse=True)
     check_all(x, cfg, out, lse=True)
+
+
+def test_sharp_attention_scores(qk):
+    """Keys and queries scaled by 4 (logits x16): sharp softmax rows whose
+    LSE sits far above most logits, where the column-max pass's lse terms and
+    fp32 cancellation matter most.  Scores below 1e-30 (fp32 exp2 flushes
+    them to zero) compare against that absolute floor."""
+    cfg = CASES["ragged-1000"]
+    x = ks.gen_kv2(cfg)
+    up = lambda b: ks.f32_to_bf16_bits(ks.bf16_bits_to_f32(b) * np.float32(4.0))
+    x = dataclasses.replace(x, K=up(x.K), Q=up(x.Q))
+    out = run_stages(qk, x, cfg, lse=True)
+    check_all(x, cfg, out, lse=True, score_floor=1e-30)
 
 
 def test_explicit_appended_keys(qk):
