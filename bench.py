@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=ks.LLAMA_16K.name, choices=list(ks.KV2_CONFIGS))
-    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use only this many layers (profiling cases)")
     ap.add_argument("--proxy", choices=["keydiff", "knorm"], default="keydiff", help="stage-1 proxy")
@@ -469,7 +469,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                "how": "pinned host inputs: K copied each step on a copy stream into one of two device buffers, "
                       "starting after the previous step's query gather (overlapping its scoring passes); query "
                       "rows and kept V rows read in place; kept indices and compacted K/V copied back to pinned "
-                      "host memory on a third stream"}
+                      "host memory on a third stream; the first step's K copy has nothing to overlap and is "
+                      "inside the timed region"}
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
