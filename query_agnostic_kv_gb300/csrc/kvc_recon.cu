@@ -566,8 +566,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
       tma_prefetch_desc(&tmApp);
       int s = 0, ab = 0;
       uint32_t bph = 0, aph = 0;
-      int issued_b[MAX_KST] = {};
-      int issued_a[2] = {0, 0};
+      int loads_b = 0, loads_a = 0;   // copies issued; copy j went to stage j % KST (buffer j % ABUF)
       // A tile t of a unit (128 rows; pass 2 reads them through the 128-row K maps)
       auto a_tile = [&](const Unit& W, int t, int32_t& y) -> const CUtensorMap* {
         if (PASS == 1) {
@@ -588,7 +587,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           tma_load_2d(dst, map, 0, y, &bars->a_full[ab]);
           tma_load_2d(dst + AHALF, map, 64, y, &bars->a_full[ab]);
         }
-        issued_a[ab]++;
+        ++loads_a;
         auto prefetch_next = [&]() {
           if (u + static_cast<int>(gridDim.x) >= P.n_units) return;
           const Unit W = decode_unit<PASS>(P, u + gridDim.x);
@@ -625,16 +624,16 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           uint8_t* dst = sB + s * BSTAGE;
           tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
           tma_load_2d(dst + BHALF, map, 64, y, &bars->b_full[s]);
-          issued_b[s]++;
+          ++loads_b;
           if (PASS == 2 && A_PREFETCH && i == min(1, U.nT - 1)) prefetch_next();
           if (++s == KST) { s = 0; bph ^= 1; }
         }
       }
       // Wait for every copy this thread started (normally already consumed).
       for (int i = 0; i < KST; ++i)
-        if (issued_b[i] > 0) mbar_wait(&bars->b_full[i], (issued_b[i] - 1) & 1, P.limit_ns);
+        if (loads_b > i) mbar_wait(&bars->b_full[i], ((loads_b - 1 - i) / KST) & 1, P.limit_ns);
       for (int i = 0; i < ABUF; ++i)
-        if (issued_a[i] > 0) mbar_wait(&bars->a_full[i], (issued_a[i] - 1) & 1, P.limit_ns);
+        if (loads_a > i) mbar_wait(&bars->a_full[i], ((loads_a - 1 - i) / ABUF) & 1, P.limit_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
