@@ -1041,6 +1041,44 @@ def run_q4(args, rank, world, local_rank):
 EPI_METRIC = "EpiCache block prefill: history tokens/s over all episodes (E * N_hist / T)"
 
 
+def epi_oracle_sample(cfg):
+    """The float64 oracle's block prefill on one KV head of layer 0 over the
+    first 8 blocks, scaled to all layers, heads and history tokens: seconds
+    per episode and a description of the sample."""
+    from oracle import kv2
+    B, S = cfg.block, cfg.sinks
+    budgets = kv2.layer_budgets(ks.gen_sensitivity(cfg).astype(np.float64), cfg.alpha, cfg.mean_budget, S)
+    Kh, Vh = ks.gen_epi_history_layer(cfg, 0)
+    Qp, Kp = ks.gen_epi_prompt_layer(cfg, 0, 0)
+    n = min(cfg.n_hist, 8 * B)
+    a = time.perf_counter()
+    kv2.block_prefill_layer(kv2.bf16_to_f64(Kh[:1, :n]), kv2.bf16_to_f64(Vh[:1, :n]),
+                            kv2.bf16_to_f64(Qp[:cfg.G]), kv2.bf16_to_f64(Kp[:1]), B, int(budgets[0]), S)
+    t = (time.perf_counter() - a) * (cfg.n_hist / n) * cfg.L * cfg.Hkv
+    return t, (f"layer 0, KV head 0, first {n} history tokens, scaled to {cfg.L} layers x {cfg.Hkv} heads x "
+               f"{cfg.n_hist} tokens")
+
+
+def epi_compact_bytes(cfg, budgets):
+    """Algorithmic bytes of the block step's compactions over one episode: an
+    over-budget layer moves its k_l kept K and V rows (read + write) and
+    their int32 positions, per KV head."""
+    B, S = cfg.block, cfg.sinks
+    nb = (cfg.n_hist + B - 1) // B
+    length = [0] * cfg.L
+    total = 0
+    for b in range(nb):
+        blk = min(B, cfg.n_hist - b * B)
+        for l in range(cfg.L):
+            n = length[l] + blk
+            if n > budgets[l] and n > S:
+                total += cfg.Hkv * budgets[l] * (2 * 2 * 128 * 2 + 2 * 4)
+                length[l] = budgets[l]
+            else:
+                length[l] = n
+    return total
+
+
 def run_epicache(args, rank, world, local_rank):
     import torch
     import query_agnostic_kv_gb300 as qk
@@ -1051,23 +1089,13 @@ def run_epicache(args, rank, world, local_rank):
     if args.impl == "reference":
         if rank != 0:
             return
-        from oracle import kv2
-        budgets = kv2.layer_budgets(ks.gen_sensitivity(cfg).astype(np.float64), cfg.alpha, cfg.mean_budget, S)
-        Kh, Vh = ks.gen_epi_history_layer(cfg, 0)
-        Qp, Kp = ks.gen_epi_prompt_layer(cfg, 0, 0)
-        n = min(cfg.n_hist, 8 * B)
-        a = time.perf_counter()
-        kv2.block_prefill_layer(kv2.bf16_to_f64(Kh[:1, :n]), kv2.bf16_to_f64(Vh[:1, :n]),
-                                kv2.bf16_to_f64(Qp[:cfg.G]), kv2.bf16_to_f64(Kp[:1]), B, int(budgets[0]), S)
-        t = (time.perf_counter() - a) * (cfg.n_hist / n) * L * H      # one KV head of one layer, scaled
+        t, sample = epi_oracle_sample(cfg)
         v = cfg.episodes * cfg.n_hist / (t * cfg.episodes)
         print(json.dumps({
             "impl": "reference", "metric": EPI_METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": 1, "warmup": 0, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": cfg.name},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
-                             "sample": f"layer 0, KV head 0, first {n} history tokens, scaled to {L} layers x {H} "
-                                       f"heads x {cfg.n_hist} tokens"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
         return
 
@@ -1136,7 +1164,73 @@ def run_epicache(args, rank, world, local_rank):
     value = world * cfg.episodes * cfg.n_hist / (ms / 1e3)
     total = sum(v[1] for v in prof.values())
     kernels = {n: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / total} for n, v in prof.items()}
+
+    # roofline of the dominant kernel: compaction, bound by HBM
+    peaks, peak_src = load_peaks()
+    hbm = peaks.get("hbm_gbs")
+    cbytes = epi_compact_bytes(cfg, budgets) * cfg.episodes
+    ctime = prof["compact"][1] / 1e3
+    ach = cbytes / ctime / 1e9
+    roof = {"kernel": "compact (kept rows of every over-budget layer into its other slab)", "bound": "hbm",
+            "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+            "peak_source": f"hbm_gbs of {peak_src} peaks",
+            "algorithmic_bytes_per_launch": cbytes / prof["compact"][0]}
+
+    # end to end: the history streamed from pinned host memory; block b is
+    # copied on a copy stream into one of two device buffers while the step
+    # of block b - 1 runs
+    e2e = None
+    if args.e2e_steps > 0:
+        hblocks = [(kb.cpu().pin_memory(), vb.cpu().pin_memory(), n) for kb, vb, n in blocks]
+        dK = [torch.empty(L * H * B * 128, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        dV = [torch.empty_like(dK[0]) for _ in range(2)]
+        cps = torch.cuda.Stream(device=dev)
+        copied = [torch.cuda.Event() for _ in range(2)]
+        free = [torch.cuda.Event() for _ in range(2)]
+        for ev in copied + free:
+            ev.record(stream)
+        torch.cuda.synchronize()
+
+        def episode_host(e, start=None):
+            st = qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0], slabs[2],
+                                         slabs[3], pos[1])
+            dq, dk = prompts[e]
+            for i, (hk, hv, n) in enumerate(hblocks):
+                j = i % 2
+                kb = dK[j][:L * H * n * 128].view(L, H, n, 128)
+                vb = dV[j][:L * H * n * 128].view(L, H, n, 128)
+                with torch.cuda.stream(cps):
+                    if start is not None and i == 0:
+                        cps.wait_event(start)
+                    cps.wait_event(free[j])
+                    kb.copy_(hk, non_blocking=True)
+                    vb.copy_(hv, non_blocking=True)
+                    copied[j].record(cps)
+                stream.wait_event(copied[j])
+                qk.kvc_block_prefill_step(st, kb, vb, n, dq, dk, P, ws=ws, stream=stream)
+                free[j].record(stream)
+
+        episode_host(0)
+        torch.cuda.synchronize()
+        a2 = torch.cuda.Event(enable_timing=True)
+        b2 = torch.cuda.Event(enable_timing=True)
+        a2.record(stream)
+        for e in range(cfg.episodes):
+            episode_host(e, start=a2 if e == 0 else None)
+        b2.record(stream)
+        torch.cuda.synchronize()
+        assert qk.kvc_stream_status() == 0
+        e_ms = a2.elapsed_time(b2)
+        h2d = sum(hk.numel() + hv.numel() for hk, hv, _ in hblocks) * 2
+        e2e = {"value": world * cfg.episodes * cfg.n_hist / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 0, "ms_per_step": e_ms / cfg.episodes,
+               "how": "history K/V blocks in pinned host memory, each copied on a copy stream into one of two device "
+                      "buffers while the previous block's step runs; the compressed cache stays on the device"}
+
     cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t, sample = epi_oracle_sample(cfg)
+        cpu = {"value": cfg.n_hist / t, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": sample}
     print(json.dumps({
         "metric": EPI_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": cfg.episodes,
         "warmup": 1, "ms_per_step": ms / cfg.episodes, "higher_is_better": True, "scaling": "weak",
@@ -1144,8 +1238,8 @@ def run_epicache(args, rank, world, local_rank):
         "config": {"workload": cfg.name, "L": L, "Hkv": H, "Hq": Hq, "n_hist": cfg.n_hist, "block": B,
                    "episodes": cfg.episodes, "prompt_queries": P, "mean_budget": cfg.mean_budget, "alpha": cfg.alpha,
                    "step": "one episode (all history blocks)", "l2": "history 10 GB on the device"},
-        "roofline": None, "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()), "clocks": clocks,
-        "e2e": None, "cpu_baseline": cpu}), flush=True)
+        "roofline": roof, "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()), "clocks": clocks,
+        "e2e": e2e, "cpu_baseline": cpu}), flush=True)
 
 
 def main():
