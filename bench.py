@@ -928,6 +928,31 @@ def run_episode(args, rank, world, local_rank):
 Q4_METRIC = "Q4 codec of a compacted KV cache: bf16 bytes encoded or restored per second"
 
 
+def q4_oracle_sample(cfg, warmup, steps):
+    """The float64 oracle's Q4 encode + decode of one segment (at most 65536
+    rows) of the workload: GB/s of bf16 rows (read and written), seconds per
+    repetition (median) and a description of the sample."""
+    from oracle import q4
+    x = ks.gen_decode(cfg, "cpu", lens=[min(cfg.kept, 65536)])
+    X = x["K"].float().numpy()
+    samples = []
+    for i in range(warmup + steps):
+        a = time.perf_counter()
+        c, sc, lo = q4.encode(X)
+        q4.decode(c, sc, lo)
+        if i >= warmup:
+            samples.append(time.perf_counter() - a)
+    t = statistics.median(samples)
+    return 2 * X.shape[0] * 256 / t / 1e9, t, f"encode + decode of {X.shape[0]} rows"
+
+
+# DRAM bytes per launch of the Q4 decode kernel as ncu counted them on the
+# 16-sequence Llama-3.1-8B 128K/10% workload (dram__bytes_read + write =
+# 241.6 + 799.3 MB); the traffic grows with the rows.  Reset to None when the
+# kernel changes until it is captured again.
+Q4_DECODE_TRAFFIC_PER_SEQ = (241.6e6 + 799.3e6) / 16
+
+
 def run_q4(args, rank, world, local_rank):
     import torch
     import query_agnostic_kv_gb300 as qk
@@ -937,19 +962,7 @@ def run_q4(args, rank, world, local_rank):
     if args.impl == "reference":
         if rank != 0:
             return
-        from oracle import q4
-        x = ks.gen_decode(cfg, "cpu", lens=[min(cfg.kept, 65536)])
-        X = x["K"].float().numpy()
-        samples = []
-        for i in range(args.warmup + args.steps):
-            a = time.perf_counter()
-            c, s, lo = q4.encode(X)
-            q4.decode(c, s, lo)
-            if i >= args.warmup:
-                samples.append(time.perf_counter() - a)
-        t = statistics.median(samples)
-        v = 2 * X.shape[0] * 256 / t / 1e9
-        desc = f"encode + decode of {X.shape[0]} rows"
+        v, t, desc = q4_oracle_sample(cfg, args.warmup, args.steps)
         print(json.dumps({
             "impl": "reference", "metric": Q4_METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
@@ -1014,6 +1027,10 @@ def run_q4(args, rank, world, local_rank):
     ach_enc = traffic / (enc_t / enc_l / 1e3) / 1e9
     ach_dec = traffic / (dec_t / dec_l / 1e3) / 1e9
     value = 2 * bf16_bytes / ((ms_enc + ms_dec) / 1e3) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, _, desc = q4_oracle_sample(cfg, 1, 3)
+        cpu = {"value": v, "unit": "GB/s", "cores": cores(), "kind": "oracle", "sample": desc}
     print(json.dumps({
         "metric": Q4_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_enc + ms_dec, "higher_is_better": True, "scaling": "weak",
@@ -1021,7 +1038,9 @@ def run_q4(args, rank, world, local_rank):
         "config": {"workload": cfg.name + "-q4", "rows": rows, "bf16_bytes": bf16_bytes, "q4_bytes": q4_bytes,
                    "l2": "inputs larger than L2; no flush between steps", "step": "one encode + one decode"},
         "roofline": {"kernel": "q4_decode", "bound": "hbm", "achieved": ach_dec, "peak": hbm, "unit": "GB/s",
-                     "frac": ach_dec / hbm, "traffic": None,
+                     "frac": ach_dec / hbm,
+                     "traffic": None if Q4_DECODE_TRAFFIC_PER_SEQ is None else Q4_DECODE_TRAFFIC_PER_SEQ * cfg.seqs,
+                     "traffic_source": "ncu dram bytes of the 16-sequence case, scaled by sequences",
                      "peak_source": "hbm_gbs of measured peaks", "algorithmic_bytes_per_launch": traffic},
         "encode": {"ms": enc_t / enc_l, "GB/s": ach_enc, "frac_of_hbm": ach_enc / hbm},
         "decode": {"ms": dec_t / dec_l, "GB/s": ach_dec, "frac_of_hbm": ach_dec / hbm},
@@ -1034,7 +1053,7 @@ def run_q4(args, rank, world, local_rank):
         "e2e": {"value": bf16_bytes / (ms_rest / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": q4_bytes,
                 "d2h_bytes_per_step": 0, "ms_per_step": ms_rest,
                 "how": "restore: the Q4 image in page-locked host memory decoded in place into device bf16 rows"},
-        "cpu_baseline": None}), flush=True)
+        "cpu_baseline": cpu}), flush=True)
 
 
 # ---------------------------------------------------------------- EpiCache block prefill leg
