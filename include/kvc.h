@@ -197,6 +197,27 @@ KVC_API kvc_status kvc_recon_score(kvc_shape shape, const void* K, const void* Q
                            int32_t m, double rho, const void* Kapp_opt, float* score, float* lse_opt, void* ws,
                            size_t ws_bytes, kvc_stream stream);
 
+/* The pages have no counterpart to these entry points: kvc_recon_score split
+ * into its three phases, for callers that overlap the phases of consecutive
+ * compression steps on several streams (for instance the next step's query
+ * gather, whose reads may cross the host link, under this step's column-max
+ * pass).  On one workspace (kvc_workspace_size) they must run in this order,
+ * on one stream or ordered by events, with the same shape, sinks, m, rho and
+ * Kapp_opt; together they compute exactly what kvc_recon_score computes.
+ *   kvc_recon_gather  fills the workspace's query rows (and, when Kapp_opt is
+ *                     NULL, the appended keys K at sel) from Qpool and sel;
+ *   kvc_recon_rows    the row log-sum-exp pass: per query row, the values the
+ *                     column-max pass subtracts; lse_opt as kvc_recon_score;
+ *   kvc_recon_cols    the column-max pass: writes score as kvc_recon_score.
+ * Arguments and errors as kvc_recon_score. */
+KVC_API kvc_status kvc_recon_gather(kvc_shape shape, const void* K, const void* Qpool, const int32_t* sel,
+                                    int32_t sinks, int32_t m, double rho, const void* Kapp_opt, void* ws,
+                                    size_t ws_bytes, kvc_stream stream);
+KVC_API kvc_status kvc_recon_rows(kvc_shape shape, const void* K, int32_t sinks, int32_t m, double rho,
+                                  const void* Kapp_opt, float* lse_opt, void* ws, size_t ws_bytes, kvc_stream stream);
+KVC_API kvc_status kvc_recon_cols(kvc_shape shape, const void* K, int32_t sinks, int32_t m, double rho, float* score,
+                                  void* ws, size_t ws_bytes, kvc_stream stream);
+
 /* KV² page, "무엇과 다른가" (iterative refinement): the stage-2 output has the
  * proxy's token granularity, so p_i = mean over the L*Hkv heads of score_i
  * replaces the proxy in the next pass.  p[i] = 0 for i < sinks.

@@ -21,7 +21,8 @@ __all__ = [
     "KVCError", "kvc_shape", "kvc_block_state", "lib", "shape_of",
     "kvc_status_string", "kvc_device_check", "kvc_stream_status", "kvc_set_wait_limit_ns",
     "kvc_debug_expire_wait", "kvc_chunk_plan", "kvc_budget_count", "kvc_workspace_size",
-    "kvc_proxy_score", "kvc_select_queries", "kvc_recon_score", "kvc_refine_proxy", "kvc_evict_topk",
+    "kvc_proxy_score", "kvc_select_queries", "kvc_recon_score", "kvc_recon_gather", "kvc_recon_rows",
+    "kvc_recon_cols", "kvc_refine_proxy", "kvc_evict_topk",
     "kvc_compact", "kvc_compress", "kvc_layer_budgets", "kvc_block_state_init",
     "kvc_block_workspace_size", "kvc_block_prefill_step", "EXPORTED",
 ]
@@ -65,6 +66,9 @@ _SIGS = {
     "kvc_select_queries": (c_i32, [c_i32, c_i32, c_i32, c_dbl, c_vp, c_vp, c_vp]),
     "kvc_recon_score": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_vp, c_vp, c_vp, c_vp, c_sz,
                                 c_vp]),
+    "kvc_recon_gather": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_recon_rows": (c_i32, [kvc_shape, c_vp, c_i32, c_i32, c_dbl, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_recon_cols": (c_i32, [kvc_shape, c_vp, c_i32, c_i32, c_dbl, c_vp, c_vp, c_sz, c_vp]),
     "kvc_refine_proxy": (c_i32, [kvc_shape, c_vp, c_i32, c_vp, c_vp]),
     "kvc_evict_topk": (c_i32, [kvc_shape, c_vp, c_i32, ctypes.POINTER(c_i32), c_vp, c_vp, c_sz, c_vp]),
     "kvc_compact": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, ctypes.POINTER(c_i32), c_vp, c_vp, c_vp]),
@@ -311,6 +315,31 @@ def kvc_recon_score(shape, K, Qpool, sel, sinks, m, rho, score, Kapp=None, lse=N
         _shape(shape), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"),
         _dev(sel, torch.int32, "sel"), sinks, m, float(rho), _dev(Kapp, torch.bfloat16, "Kapp"),
         _dev(score, torch.float32, "score"), _dev(lse, torch.float32, "lse"), w, wb, _stream(stream)))
+
+
+def kvc_recon_gather(shape, K, Qpool, sel, sinks, m, rho, Kapp=None, ws=None, stream=None) -> None:
+    """Phase 1 of kvc_recon_score: the query rows (and appended keys) into the workspace."""
+    w, wb = _ws(ws)
+    _check("kvc_recon_gather", lib().kvc_recon_gather(
+        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"),
+        _dev(sel, torch.int32, "sel"), sinks, m, float(rho), _dev(Kapp, torch.bfloat16, "Kapp"), w, wb,
+        _stream(stream)))
+
+
+def kvc_recon_rows(shape, K, sinks, m, rho, Kapp=None, lse=None, ws=None, stream=None) -> None:
+    """Phase 2 of kvc_recon_score: the row log-sum-exp pass."""
+    w, wb = _ws(ws)
+    _check("kvc_recon_rows", lib().kvc_recon_rows(
+        _shape(shape), _dev(K, torch.bfloat16, "K"), sinks, m, float(rho), _dev(Kapp, torch.bfloat16, "Kapp"),
+        _dev(lse, torch.float32, "lse"), w, wb, _stream(stream)))
+
+
+def kvc_recon_cols(shape, K, sinks, m, rho, score, ws=None, stream=None) -> None:
+    """Phase 3 of kvc_recon_score: the column-max pass, writing score."""
+    w, wb = _ws(ws)
+    _check("kvc_recon_cols", lib().kvc_recon_cols(
+        _shape(shape), _dev(K, torch.bfloat16, "K"), sinks, m, float(rho), _dev(score, torch.float32, "score"),
+        w, wb, _stream(stream)))
 
 
 def kvc_refine_proxy(shape, score, sinks, p, stream=None) -> None:

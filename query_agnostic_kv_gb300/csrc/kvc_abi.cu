@@ -295,9 +295,13 @@ kvc_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 
 cudaStream_t cs(kvc_stream s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Caller-supplied appended keys are a tensor-map source like K: device
+// memory, 16-byte aligned (or absent).
+bool kapp_ok(const void* Kapp) { return !Kapp || (aligned16(Kapp) && is_device_memory(Kapp)); }
+
 kvc_status run_recon(const kvc_shape& s, const ChunkPlan& plan, int32_t sinks, const void* K, const void* Qpool,
                      const int32_t* sel, const void* Kapp, float* score, float* lse_out, const KV2Workspace& w,
-                     cudaStream_t st, cudaEvent_t gather_done = nullptr) {
+                     cudaStream_t st, cudaEvent_t gather_done = nullptr, int phases = RECON_ALL) {
   ReconProblem pr;
   memset(&pr, 0, sizeof(pr));
   pr.L = s.L;
@@ -329,7 +333,7 @@ kvc_status run_recon(const kvc_shape& s, const ChunkPlan& plan, int32_t sinks, c
   pr.ldS = s.N;
   pr.lse_out = lse_out;
   pr.gather_done = gather_done;
-  return cuda_status(launch_recon(pr, w.rw, st));
+  return cuda_status(launch_recon(pr, w.rw, st, phases));
 }
 
 kvc_status run_evict(const kvc_shape& s, float* score, int32_t sinks, const int32_t* k_per_layer, int32_t* kept,
@@ -525,9 +529,8 @@ kvc_status kvc_recon_score(kvc_shape shape, const void* K, const void* Qpool, co
                            size_t ws_bytes, kvc_stream stream) {
   ChunkPlan plan;
   if (!shape_ok(shape) || !K || !Qpool || !sel || !score || !aligned16(K) || !aligned16(Qpool) ||
-      !is_device_memory(K) || !device_can_read(Qpool) ||
-      (Kapp_opt && !aligned16(Kapp_opt)) || !make_plan(shape.N, sinks, m, rho, &plan) ||
-      !reachable(sel, score, lse_opt, Kapp_opt, ws))
+      !is_device_memory(K) || !device_can_read(Qpool) || !kapp_ok(Kapp_opt) ||
+      !make_plan(shape.N, sinks, m, rho, &plan) || !reachable(sel, score, lse_opt, ws))
     return KVC_ERR_INVALID;
   KV2Workspace w = carve_kv2(shape, plan, ws, ws_bytes);
   kvc_status e = check_ws(ws, ws_bytes, w.bytes);
@@ -535,6 +538,53 @@ kvc_status kvc_recon_score(kvc_shape shape, const void* K, const void* Qpool, co
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
   return run_recon(shape, plan, sinks, K, Qpool, sel, Kapp_opt, score, lse_opt, w, cs(stream));
+}
+
+kvc_status kvc_recon_gather(kvc_shape shape, const void* K, const void* Qpool, const int32_t* sel, int32_t sinks,
+                            int32_t m, double rho, const void* Kapp_opt, void* ws, size_t ws_bytes,
+                            kvc_stream stream) {
+  ChunkPlan plan;
+  if (!shape_ok(shape) || !K || !Qpool || !sel || !aligned16(K) || !aligned16(Qpool) || !is_device_memory(K) ||
+      !device_can_read(Qpool) || !kapp_ok(Kapp_opt) || !make_plan(shape.N, sinks, m, rho, &plan) ||
+      !reachable(sel, ws))
+    return KVC_ERR_INVALID;
+  KV2Workspace w = carve_kv2(shape, plan, ws, ws_bytes);
+  kvc_status e = check_ws(ws, ws_bytes, w.bytes);
+  if (e != KVC_OK || !w.ok) return KVC_ERR_WORKSPACE;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return run_recon(shape, plan, sinks, K, Qpool, sel, Kapp_opt, nullptr, nullptr, w, cs(stream), nullptr,
+                   RECON_GATHER);
+}
+
+kvc_status kvc_recon_rows(kvc_shape shape, const void* K, int32_t sinks, int32_t m, double rho, const void* Kapp_opt,
+                          float* lse_opt, void* ws, size_t ws_bytes, kvc_stream stream) {
+  ChunkPlan plan;
+  if (!shape_ok(shape) || !K || !aligned16(K) || !is_device_memory(K) || !kapp_ok(Kapp_opt) ||
+      !make_plan(shape.N, sinks, m, rho, &plan) || !reachable(lse_opt, ws))
+    return KVC_ERR_INVALID;
+  KV2Workspace w = carve_kv2(shape, plan, ws, ws_bytes);
+  kvc_status e = check_ws(ws, ws_bytes, w.bytes);
+  if (e != KVC_OK || !w.ok) return KVC_ERR_WORKSPACE;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return run_recon(shape, plan, sinks, K, nullptr, nullptr, Kapp_opt, nullptr, lse_opt, w, cs(stream), nullptr,
+                   RECON_ROWS);
+}
+
+kvc_status kvc_recon_cols(kvc_shape shape, const void* K, int32_t sinks, int32_t m, double rho, float* score,
+                          void* ws, size_t ws_bytes, kvc_stream stream) {
+  ChunkPlan plan;
+  if (!shape_ok(shape) || !K || !score || !aligned16(K) || !is_device_memory(K) ||
+      !make_plan(shape.N, sinks, m, rho, &plan) || !reachable(score, ws))
+    return KVC_ERR_INVALID;
+  KV2Workspace w = carve_kv2(shape, plan, ws, ws_bytes);
+  kvc_status e = check_ws(ws, ws_bytes, w.bytes);
+  if (e != KVC_OK || !w.ok) return KVC_ERR_WORKSPACE;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return run_recon(shape, plan, sinks, K, nullptr, nullptr, nullptr, score, nullptr, w, cs(stream), nullptr,
+                   RECON_COLS);
 }
 
 kvc_status kvc_refine_proxy(kvc_shape shape, const float* score, int32_t sinks, float* p, kvc_stream stream) {

@@ -169,7 +169,11 @@ struct ReconWorkspace {
 };
 // Rows per (layer, KV head) of the query row space (chunks padded to 128 rows).
 int32_t recon_rows(int G, int n_chunks, int nq_full, int nq_last);
-cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaStream_t st);
+// Phases of the scoring (bit mask): query gather into the row space, the
+// row-LSE pass, the column-max pass.  They run in that order on one
+// workspace; a call may run any contiguous subset of them.
+enum : int { RECON_GATHER = 1, RECON_ROWS = 2, RECON_COLS = 4, RECON_ALL = 7 };
+cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaStream_t st, int phases = RECON_ALL);
 
 // Device-side wait that expires on purpose (status-path test).
 cudaError_t launch_expire_wait(uint64_t limit_ns, cudaStream_t st);

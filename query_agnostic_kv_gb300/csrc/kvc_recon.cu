@@ -955,7 +955,7 @@ int32_t recon_rows(int G, int n_chunks, int nq_full, int nq_last) {
   return (n_chunks - 1) * CR + round_up(G * nq_last, TILE_ROWS);
 }
 
-cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaStream_t st) {
+cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaStream_t st, int phases) {
   const int G = pr.G;
   // chunk layout is the same for every active layer in one call
   const int nc0 = pr.lay[0].n_chunks;
@@ -964,48 +964,51 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   if (Rpad != ws.Rpad) return cudaErrorInvalidValue;
 
   // ---- gather
-  GParams gp;
-  memset(&gp, 0, sizeof(gp));
-  gp.Hkv = pr.Hkv; gp.Hq = pr.Hq; gp.G = G; gp.n_active = pr.n_active;
-  for (int a = 0; a < pr.n_active; ++a) {
-    gp.layer[a] = pr.lay[a].layer;
-    gp.n[a] = pr.lay[a].n;
-    gp.slab[a] = pr.lay[a].slab;
-    gp.n_chunks[a] = pr.lay[a].n_chunks;
-  }
-  gp.nq_full = pr.nq_full; gp.nq_last = pr.nq_last; gp.Q = pr.Q; gp.CR = CR; gp.Rpad = Rpad;
-  gp.sel = pr.sel;
-  gp.Qsrc = static_cast<const __nv_bfloat16*>(pr.Qsrc);
-  gp.ldQ = pr.ldQ;
-  gp.K[0] = static_cast<const __nv_bfloat16*>(pr.K[0]);
-  gp.K[1] = static_cast<const __nv_bfloat16*>(pr.K[1] ? pr.K[1] : pr.K[0]);
-  gp.ldK = pr.ldK;
-  gp.Qg = static_cast<__nv_bfloat16*>(ws.Qg);
-  gp.Kg = pr.Kapp ? nullptr : static_cast<__nv_bfloat16*>(ws.Kg);
-  gp.status = status_word();
-  {
-    const int64_t rows = static_cast<int64_t>(pr.n_active) * pr.Hkv * (Rpad + (gp.Kg ? pr.Q : 0));
-    int64_t blocks = (rows + 63) / 64;
-    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+  if (phases & RECON_GATHER) {
+    GParams gp;
+    memset(&gp, 0, sizeof(gp));
+    gp.Hkv = pr.Hkv; gp.Hq = pr.Hq; gp.G = G; gp.n_active = pr.n_active;
+    for (int a = 0; a < pr.n_active; ++a) {
+      gp.layer[a] = pr.lay[a].layer;
+      gp.n[a] = pr.lay[a].n;
+      gp.slab[a] = pr.lay[a].slab;
+      gp.n_chunks[a] = pr.lay[a].n_chunks;
+    }
+    gp.nq_full = pr.nq_full; gp.nq_last = pr.nq_last; gp.Q = pr.Q; gp.CR = CR; gp.Rpad = Rpad;
+    gp.sel = pr.sel;
+    gp.Qsrc = static_cast<const __nv_bfloat16*>(pr.Qsrc);
+    gp.ldQ = pr.ldQ;
+    gp.K[0] = static_cast<const __nv_bfloat16*>(pr.K[0]);
+    gp.K[1] = static_cast<const __nv_bfloat16*>(pr.K[1] ? pr.K[1] : pr.K[0]);
+    gp.ldK = pr.ldK;
+    gp.Qg = static_cast<__nv_bfloat16*>(ws.Qg);
+    gp.Kg = pr.Kapp ? nullptr : static_cast<__nv_bfloat16*>(ws.Kg);
+    gp.status = status_word();
     {
-      ProfScope ps("recon_gather", st);
-      // 32-bit row arithmetic while every index (plus one grid stride of
-      // look-ahead) stays below 2^31
-      const int64_t slack = blocks * 16 * 4 * 2;
-      if (rows + slack < (int64_t(1) << 31))
-        gather_kernel<int, 4><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
-      else
-        gather_kernel<int64_t, 4><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (pr.gather_done) {
-      e = cudaEventRecord(pr.gather_done, st);
+      const int64_t rows = static_cast<int64_t>(pr.n_active) * pr.Hkv * (Rpad + (gp.Kg ? pr.Q : 0));
+      int64_t blocks = (rows + 63) / 64;
+      const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+      if (blocks > cap) blocks = cap;
+      if (blocks < 1) blocks = 1;
+      {
+        ProfScope ps("recon_gather", st);
+        // 32-bit row arithmetic while every index (plus one grid stride of
+        // look-ahead) stays below 2^31
+        const int64_t slack = blocks * 16 * 4 * 2;
+        if (rows + slack < (int64_t(1) << 31))
+          gather_kernel<int, 4><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
+        else
+          gather_kernel<int64_t, 4><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
+      }
+      cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
+      if (pr.gather_done) {
+        e = cudaEventRecord(pr.gather_done, st);
+        if (e != cudaSuccess) return e;
+      }
     }
   }
+  if (!(phases & (RECON_ROWS | RECON_COLS))) return cudaSuccess;
 
   // ---- tensor maps
   // Rows are addressed by model layer index, so the maps span all L layers.
@@ -1060,7 +1063,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   const int sms = num_sms();
   // pass 1
   kp.n_units = pr.n_active * pr.Hkv * kp.units1;
-  if (kp.n_units > 0) {
+  if ((phases & RECON_ROWS) && kp.n_units > 0) {
     ProfScope ps("recon_lse", st);
     recon_kernel<1><<<kp.n_units < sms ? kp.n_units : sms, kThreads<1>, kSmemBytes<1>, st>>>(tmQg, tmK0b, tmK1b,
                                                                                             tmApp, kp);
@@ -1069,7 +1072,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   }
   // pass 2
   kp.n_units = acc;
-  if (kp.n_units > 0) {
+  if ((phases & RECON_COLS) && kp.n_units > 0) {
     ProfScope ps("recon_colmax", st);
     recon_kernel<2><<<kp.n_units < sms ? kp.n_units : sms, kThreads<2>, kSmemBytes<2>, st>>>(tmQgB, tmK0a, tmK1a,
                                                                                             tmLx, kp);

@@ -148,6 +148,44 @@ def test_sharp_attention_scores(qk):
     check_all(x, cfg, out, lse=True, score_floor=1e-30)
 
 
+@pytest.mark.parametrize("name", ["ragged-1000", "tiny-4k"])
+def test_recon_phases_match_one_call(qk, name):
+    """kvc_recon_gather, kvc_recon_rows and kvc_recon_cols on one workspace
+    (the gather on a second stream, ordered by an event) give exactly
+    kvc_recon_score's scores and lse."""
+    cfg = CASES[name]
+    x = ks.gen_kv2(cfg)
+    L, H, Hq, N, S = cfg.L, cfg.Hkv, cfg.Hq, cfg.N, cfg.sinks
+    shape = (L, H, Hq, 128, N)
+    K, Q = to_dev(x.K), to_dev(x.Q)
+    Qn = qk.kvc_chunk_plan(N, S, cfg.m, cfg.rho)[-1]
+    wsz = qk.kvc_workspace_size(shape, S, cfg.m, cfg.rho)
+    ws1 = torch.empty(wsz, dtype=torch.uint8, device=DEV)
+    ws2 = torch.empty(wsz, dtype=torch.uint8, device=DEV)
+    p = torch.empty(N, dtype=torch.float32, device=DEV)
+    qk.kvc_proxy_score(shape, K, p, ws=ws1)
+    sel = torch.empty(Qn, dtype=torch.int32, device=DEV)
+    qk.kvc_select_queries(N, S, cfg.m, cfg.rho, p, sel)
+    score1 = torch.full((L * H * N,), float("nan"), device=DEV)
+    lse1 = torch.empty(L * Hq * Qn, device=DEV)
+    qk.kvc_recon_score(shape, K, Q, sel, S, cfg.m, cfg.rho, score1, lse=lse1, ws=ws1)
+    score2 = torch.full_like(score1, float("nan"))
+    lse2 = torch.empty_like(lse1)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=DEV)
+    side.wait_stream(main)
+    with torch.cuda.stream(side):
+        qk.kvc_recon_gather(shape, K, Q, sel, S, cfg.m, cfg.rho, ws=ws2, stream=side)
+        done = torch.cuda.Event()
+        done.record(side)
+    main.wait_event(done)
+    qk.kvc_recon_rows(shape, K, S, cfg.m, cfg.rho, lse=lse2, ws=ws2)
+    qk.kvc_recon_cols(shape, K, S, cfg.m, cfg.rho, score2, ws=ws2)
+    assert qk.kvc_stream_status() == 0
+    assert torch.equal(score1.view(L, H, N)[:, :, S:], score2.view(L, H, N)[:, :, S:])
+    assert torch.equal(lse1, lse2)
+
+
 def test_explicit_appended_keys(qk):
     """Appended keys supplied by the caller (e.g. from a real reconstruction
     forward) instead of the cache keys at the selected positions."""
