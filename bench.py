@@ -386,6 +386,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     # ---- end to end through the public API with host buffers
     e2e = None
     if args.e2e_steps > 0:
+        kept_ref = kept.cpu()              # the device-resident run's result, for the check below
         hK = torch.from_numpy(x.K.view(np.int16)).view(torch.bfloat16).pin_memory()
         hV = torch.from_numpy(x.V.view(np.int16)).view(torch.bfloat16).pin_memory()
         hQ = torch.from_numpy(x.Q.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -442,6 +443,83 @@ def run_ours(args, cfg, rank, world, local_rank):
                     ev_out[bsel].record(d2h_stream)
             stream.wait_stream(d2h_stream)
 
+        # Single-pass steps run through the three scoring phases instead, so
+        # that consecutive steps overlap: while step i's row pass runs, step
+        # i+1's K copy finishes; step i+1's proxy and selection then run (the
+        # whole GPU), and its query gather -- reads across the host link --
+        # runs beside step i's column pass (its blocks fit beside the
+        # column-max CTAs); step i+2's K copy follows that gather.  Each step
+        # alternates between two workspaces and output sets.  The host
+        # enqueues in dependency order, so every event a stream waits on has
+        # already been recorded for that step.
+        if cfg.passes == 1:
+            wsb = [ws, torch.empty_like(ws)]
+            pb = [torch.empty(N, dtype=torch.float32, device=dev) for _ in range(2)]
+            selb = [torch.empty(work["Q"], dtype=torch.int32, device=dev) for _ in range(2)]
+            scoreb = [torch.empty(L * H * N, dtype=torch.float32, device=dev) for _ in range(2)]
+            prep_stream = torch.cuda.Stream(device=dev)
+            ev_sel = [torch.cuda.Event(), torch.cuda.Event()]
+            ev_gath = [torch.cuda.Event(), torch.cuda.Event()]
+            ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+            for evs in (ev_sel, ev_gath, ev_done):
+                for ev in evs:
+                    ev.record(stream)
+            torch.cuda.synchronize()
+
+            def copy_k(i, after):
+                with torch.cuda.stream(copy_stream):
+                    for ev in after:
+                        copy_stream.wait_event(ev)
+                    Kbuf[i % 2].copy_(hK, non_blocking=True)
+                    ev_copied[i % 2].record(copy_stream)
+
+            def prep_front(i):        # proxy and selection of step i
+                b = i % 2
+                with torch.cuda.stream(prep_stream):
+                    prep_stream.wait_event(ev_copied[b])
+                    if i >= 2:
+                        prep_stream.wait_event(ev_done[b])   # workspace b: step i-2 is done with it
+                    qk.kvc_proxy_score_kind(shape, args.proxy, Kbuf[b], pb[b], ws=wsb[b], stream=prep_stream)
+                    qk.kvc_select_queries(N, S, cfg.m, cfg.rho, pb[b], selb[b], stream=prep_stream)
+                    ev_sel[b].record(prep_stream)
+
+            def prep_back(i):         # query gather of step i
+                b = i % 2
+                with torch.cuda.stream(prep_stream):
+                    qk.kvc_recon_gather(shape, Kbuf[b], hQ, selb[b], S, cfg.m, cfg.rho, ws=wsb[b],
+                                        stream=prep_stream)
+                    ev_gath[b].record(prep_stream)
+
+            def e2e_steps(n, start_event=None):
+                copy_k(0, [start_event] if start_event is not None else [])
+                prep_front(0)
+                prep_back(0)
+                if n > 1:
+                    copy_k(1, [ev_gath[0]])
+                for i in range(n):
+                    b = i % 2
+                    stream.wait_event(ev_gath[b])
+                    qk.kvc_recon_rows(shape, Kbuf[b], S, cfg.m, cfg.rho, ws=wsb[b], stream=stream)
+                    if i + 1 < n:
+                        prep_front(i + 1)
+                        stream.wait_event(ev_sel[(i + 1) % 2])
+                    qk.kvc_recon_cols(shape, Kbuf[b], S, cfg.m, cfg.rho, scoreb[b], ws=wsb[b], stream=stream)
+                    if i + 1 < n:
+                        prep_back(i + 1)
+                    stream.wait_event(ev_out[b])                 # host copies of step i-2 are done
+                    qk.kvc_evict_topk(shape, scoreb[b], S, kl, kept2[b], ws=wsb[b], stream=stream)
+                    qk.kvc_compact(shape, Kbuf[b], hV, kept2[b], kl, Kc2[b], Vc2[b], stream=stream)
+                    ev_done[b].record(stream)
+                    if i + 2 < n:
+                        copy_k(i + 2, [ev_gath[(i + 1) % 2], ev_done[b]])
+                    with torch.cuda.stream(d2h_stream):
+                        d2h_stream.wait_event(ev_done[b])
+                        hkept[b].copy_(kept2[b], non_blocking=True)
+                        hKc[b].copy_(Kc2[b], non_blocking=True)
+                        hVc[b].copy_(Vc2[b], non_blocking=True)
+                        ev_out[b].record(d2h_stream)
+                stream.wait_stream(d2h_stream)
+
         e2e_steps(2)
         torch.cuda.synchronize()
         if world > 1:
@@ -460,17 +538,25 @@ def run_ours(args, cfg, rank, world, local_rank):
         st = qk.kvc_stream_status(stream)
         if st != 0:
             raise RuntimeError(f"device status after e2e steps: {qk.kvc_status_string(st)}")
+        # every step compresses the same inputs: the last one must match the device-resident run
+        if not torch.equal(hkept[(args.e2e_steps - 1) % 2], kept_ref):
+            raise RuntimeError("end-to-end steps kept other positions than the device-resident run")
         # bytes crossing host -> device per step: K copied, plus the query rows
         # and kept V rows the kernels read from mapped host memory
         h2d = hK.numel() * 2 + cfg.passes * L * Hq * work["Q"] * d * 2 + L * H * k * d * 2
         d2h = hkept[0].numel() * 4 + (hKc[0].numel() + hVc[0].numel()) * 2
         e2e = {"value": world * N * args.e2e_steps / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.e2e_steps,
-               "how": "pinned host inputs: K copied each step on a copy stream into one of two device buffers, "
-                      "starting after the previous step's query gather (overlapping its scoring passes); query "
-                      "rows and kept V rows read in place; kept indices and compacted K/V copied back to pinned "
-                      "host memory on a third stream; the first step's K copy has nothing to overlap and is "
-                      "inside the timed region"}
+               "how": ("pinned host inputs: K copied each step on a copy stream into one of two device buffers; "
+                       "query rows and kept V rows read in place; kept indices and compacted K/V copied back to "
+                       "pinned host memory on another stream; " +
+                       ("the scoring phases of consecutive steps overlap: the next step's proxy, selection and "
+                        "query gather run on a second stream, the gather beside this step's column-max pass, and "
+                        "the K copy after that gather, under the next row pass"
+                        if cfg.passes == 1 else
+                        "each K copy starts after the previous step's query gather, under its scoring passes") +
+                       "; the first step's K copy and preparation have nothing to overlap and are inside the timed "
+                       "region")}
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
