@@ -55,11 +55,11 @@ constexpr int SMEM_BYTES = CACHE_ROWS * 256 + HALVES * 128 * 4;
 
 // ---------------------------------------------------------------------------
 // Per-row arithmetic of the KeyDiff kernel.  Channel products run on packed
-// f32x2 pairs (measured 0.31 ms against 0.39 ms with scalar FMAs at 16K), and
-// the eight rows a half-warp has in flight are reduced
-// together: a transposing butterfly leaves row u's total on lanes 2u and
-// 2u+1 of the half-warp after 15 shuffles for all eight rows (a butterfly per
-// row takes 32).
+// f32x2 pairs (measured 0.31 ms against 0.39 ms with scalar FMAs at 16K),
+// and the eight rows a half-warp has in flight are reduced together: a
+// transposing butterfly leaves row u's total on lanes 2u and 2u+1 of the
+// half-warp after 15 shuffles for all eight rows (a butterfly per row takes
+// 32).
 __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
   return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
