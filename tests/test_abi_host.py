@@ -92,6 +92,22 @@ def test_invalid_arguments_rejected_on_host(qk):
     assert qk.kvc_workspace_size((1, 1, 4, 128, 4096), 4, 1024, 0.1) > 0
 
 
+def test_scoring_phases_reject_bad_arguments_on_host(qk):
+    """The three scoring phases check their arguments before any device call:
+    a missing pointer or a shape with d != 128 returns KVC_ERR_INVALID."""
+    lib = qk.lib()
+    sh = qk.kvc_shape(1, 1, 4, 128, 4096)
+    assert lib.kvc_recon_gather(sh, None, None, None, 4, 1024, 0.1, None, None, 0, None) == 1
+    assert lib.kvc_recon_rows(sh, None, 4, 1024, 0.1, None, None, None, 0, None) == 1
+    assert lib.kvc_recon_cols(sh, None, 4, 1024, 0.1, None, None, 0, None) == 1
+    bad = qk.kvc_shape(1, 1, 4, 64, 4096)
+    fake = 1 << 20      # never dereferenced: the shape is rejected first
+    assert lib.kvc_recon_gather(bad, fake, fake, fake, 4, 1024, 0.1, None, fake, 1 << 30, None) == 1
+    assert lib.kvc_recon_rows(bad, fake, 4, 1024, 0.1, None, None, fake, 1 << 30, None) == 1
+    assert lib.kvc_recon_cols(bad, fake, 4, 1024, 0.1, fake, fake, 1 << 30, None) == 1
+    assert lib.kvc_recon_cols(sh, fake, 4, 1024, 1.5, fake, fake, 1 << 30, None) == 1   # rho > 1
+
+
 def test_compact_segments_match_oracle(qk):
     from oracle import decode
     kl = [7, 0, 12, 3]
