@@ -94,12 +94,13 @@ def algorithmic_work(cfg):
             "bytes": b, "flops_lse_per_launch": f_lse, "flops_colmax_per_launch": f_col}
 
 
-# DRAM bytes per launch of the row-LSE kernel as ncu counted them on the
-# 4-layer case of the 16K workload (dram__bytes_read + dram__bytes_write =
-# 202.30 + 7.37 MB; the writes are mostly the 32-byte lse rows the column-max
-# pass reads); the traffic grows with the number of (layer, KV head) pairs.
-# Reset to None whenever the kernel changes until it is captured again.
-LSE_TRAFFIC_PER_LAYER = (202.30e6 + 7.37e6) / 4
+# DRAM bytes per launch of the row-LSE kernel as ncu counted them (one pass,
+# no replay) on the 4-layer case of the 16K workload: dram__bytes_read +
+# dram__bytes_write = 202.27 + 3.82 MB (the writes are the 32-byte lse rows
+# the column-max pass reads, part of them still in L2 when the kernel ends);
+# the traffic grows with the number of (layer, KV head) pairs.  Reset to None
+# whenever the kernel changes until it is captured again.
+LSE_TRAFFIC_PER_LAYER = (202.27e6 + 3.82e6) / 4
 
 
 def load_peaks():
