@@ -124,6 +124,9 @@ CASES = {
                                 sinks=3, needles_per_layer=2),
     "tiny-nq1": ks.scaled(ks.TINY, name="nq1", L=1, Hkv=1, Hq=4, N=300, m=40, rho=0.001, budget=0.05,
                           needles_per_layer=0),
+    # G = 8 (304 query rows per chunk: two column-max query tiles, the second ragged) and no sinks
+    "g8-no-sinks": ks.scaled(ks.TINY, name="g8s0", L=1, Hkv=2, Hq=16, N=900, m=256, rho=0.15, budget=0.1, sinks=0,
+                             needles_per_layer=3),
 }
 
 
