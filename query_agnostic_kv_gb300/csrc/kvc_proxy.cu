@@ -52,6 +52,12 @@ constexpr int CACHE_ROWS = KVC_KD_CACHE;  // rows of the slice kept in shared me
 // likeliest to still be in L2, and the first rows come from the cache.
 constexpr bool PASS_B_REVERSE = KVC_KD_REVERSE != 0;
 constexpr int SMEM_BYTES = CACHE_ROWS * 256 + HALVES * 128 * 4;
+#ifndef KVC_KD_PREFETCH
+#define KVC_KD_PREFETCH 1
+#endif
+// Steps ahead of the L2 prefetch of rows (0: none).  16K workload: none
+// 0.311 ms, one step 0.302, two 0.355, three 0.388 (registers spill).
+constexpr int KD_PREFETCH = KVC_KD_PREFETCH;
 
 // ---------------------------------------------------------------------------
 // Per-row arithmetic of the KeyDiff kernel.  Channel products run on packed
@@ -148,6 +154,11 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
       const int i = base + u * HALVES + hw;
       q[u] = (i < i1) ? __ldg(rows + static_cast<int64_t>(i) * 16 + l16) : make_uint4(0, 0, 0, 0);
     }
+    if (KD_PREFETCH) {
+      // warm L2 with the rows KD_PREFETCH steps ahead: lane l16 takes line (l16 & 1) of row (l16 >> 1)
+      const int i = base + KD_PREFETCH * HALVES * UNROLL + u_own * HALVES + hw;
+      if (i < i1) prefetch_l2(rows + static_cast<int64_t>(i) * 16 + (l16 & 1) * 8);
+    }
     float ss[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
@@ -207,6 +218,12 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
   for (int bi = 0; bi < nblk; ++bi) {
     const int base = i0 + (PASS_B_REVERSE ? nblk - 1 - bi : bi) * HALVES * UNROLL;
     const int i_own = base + u_own * HALVES + hw;
+    if (KD_PREFETCH && bi + KD_PREFETCH < nblk) {
+      // the rows KD_PREFETCH steps ahead that are not in the shared-memory copy
+      const int nb = i0 + (PASS_B_REVERSE ? nblk - 1 - bi - KD_PREFETCH : bi + KD_PREFETCH) * HALVES * UNROLL;
+      const int i = nb + u_own * HALVES + hw;
+      if (i < i1 && i - i0 >= CACHE_ROWS) prefetch_l2(rows + static_cast<int64_t>(i) * 16 + (l16 & 1) * 8);
+    }
     // 1/|k| of the owned row, written by this same lane in pass A
     const float inv_own = (writer && i_own < i1) ? srow[i_own] : 0.f;
     uint4 q[UNROLL];
