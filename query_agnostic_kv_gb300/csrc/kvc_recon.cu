@@ -853,8 +853,8 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
 
 // ----------------------------------------------------------------- gather
 // Fill the row space Qg (query rows, zero padding) and, for KV², the
-// appended keys Kg = K[l, h, sel].  Half a warp moves one 256-byte row; each
-// half-warp has four rows in flight.
+// appended keys Kg = K[l, h, sel]: 256-byte rows, copied by half-warps
+// (gather_rows_kernel).
 struct GParams {
   int Hkv, Hq, G;
   int n_active;
@@ -897,7 +897,7 @@ __device__ __forceinline__ void gather_row(const GParams& P, I w, I rows_q, cons
       if (s >= 0 && s < P.ldQ)
         src = reinterpret_cast<const uint4*>(
             P.Qsrc + ((static_cast<int64_t>(layer) * P.Hq + h * P.G + g) * P.ldQ + s) * kHeadDim);
-      else if ((threadIdx.x & 15) == 0)
+      else
         record_status(P.status, DEV_BOUNDS);
     }
   } else {
@@ -913,36 +913,47 @@ __device__ __forceinline__ void gather_row(const GParams& P, I w, I rows_q, cons
     if (s >= 0 && s < P.n[ai])
       src = reinterpret_cast<const uint4*>(P.K[P.slab[ai]] +
                                            ((static_cast<int64_t>(layer) * P.Hkv + h) * P.ldK + s) * kHeadDim);
-    else if ((threadIdx.x & 15) == 0)
+    else
       record_status(P.status, DEV_BOUNDS);
   }
 }
 
-template <class I, int ROWS>
-__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GParams P) {
+// Lane `sub` of a half-warp resolves row w0 + sub of 16 consecutive rows (one
+// set of index divisions per row; with every lane resolving the same row the
+// gather took 45% longer), and the half-warp then copies them four at a time,
+// taking each row's addresses by shuffle: 16 lanes x 16 bytes per 256-byte
+// row, four rows in flight.  Half-warps run independent loops, so the
+// shuffles name only their own 16 lanes.
+template <class I>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant__ GParams P) {
   const I rows_q = static_cast<I>(P.n_active) * P.Hkv * P.Rpad;
   const I rows_k = P.Kg ? static_cast<I>(P.n_active) * P.Hkv * P.Q : 0;
   const I total = rows_q + rows_k;
   const int sub = threadIdx.x & 15;
+  const unsigned hmask = 0xffffu << (threadIdx.x & 16);
   const I hw = static_cast<I>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4);
-  const I stride = static_cast<I>(gridDim.x) * (blockDim.x >> 4);
-  for (I w0 = hw; w0 < total; w0 += stride * ROWS) {
-    uint4 val[ROWS];
-    uint4* dst[ROWS];
+  const I stride = static_cast<I>(gridDim.x) * (blockDim.x >> 4) * 16;
+  for (I w0 = hw * 16; w0 < total; w0 += stride) {
+    const uint4* src = nullptr;
+    uint4* dst = nullptr;
+    const I w = w0 + sub;
+    if (w < total) gather_row(P, w, rows_q, src, dst);
+    const unsigned long long s64 = reinterpret_cast<unsigned long long>(src);
+    const unsigned long long d64 = reinterpret_cast<unsigned long long>(dst);
 #pragma unroll
-    for (int u = 0; u < ROWS; ++u) {
-      const I w = w0 + u * stride;
-      dst[u] = nullptr;
-      val[u] = make_uint4(0, 0, 0, 0);
-      if (w < total) {
-        const uint4* src;
-        gather_row(P, w, rows_q, src, dst[u]);
-        if (src) val[u] = __ldg(src + sub);
+    for (int b = 0; b < 16; b += 4) {
+      uint4 val[4];
+      uint4* d[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4* sr = reinterpret_cast<const uint4*>(__shfl_sync(hmask, s64, b + u, 16));
+        d[u] = reinterpret_cast<uint4*>(__shfl_sync(hmask, d64, b + u, 16));
+        val[u] = sr ? __ldg(sr + sub) : make_uint4(0, 0, 0, 0);
       }
-    }
 #pragma unroll
-    for (int u = 0; u < ROWS; ++u)
-      if (dst[u]) dst[u][sub] = val[u];
+      for (int u = 0; u < 4; ++u)
+        if (d[u]) d[u][sub] = val[u];
+    }
   }
 }
 
@@ -994,11 +1005,11 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
         ProfScope ps("recon_gather", st);
         // 32-bit row arithmetic while every index (plus one grid stride of
         // look-ahead) stays below 2^31
-        const int64_t slack = blocks * 16 * 4 * 2;
+        const int64_t slack = blocks * 16 * 16 * 2;
         if (rows + slack < (int64_t(1) << 31))
-          gather_kernel<int, 4><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
+          gather_rows_kernel<int><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
         else
-          gather_kernel<int64_t, 4><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
+          gather_rows_kernel<int64_t><<<static_cast<int>(blocks), 256, 0, st>>>(gp);
       }
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
