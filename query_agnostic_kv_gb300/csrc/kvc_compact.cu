@@ -22,11 +22,21 @@ __global__ void __launch_bounds__(THREADS) compact_kernel(const uint4* __restric
                                                           int32_t* __restrict__ pos_dst, uint4* __restrict__ Kc,
                                                           uint4* __restrict__ Vc,
                                                           const __grid_constant__ CompactParams P, int* status) {
-  const int l = blockIdx.z, h = blockIdx.y;
-  if (!P.active[l]) return;
+  // One block per (layer, KV head, 64-row tile) of the active layers only:
+  // layer l owns blocks [unit_off[l], unit_off[l+1]), head-major.  Budgets
+  // that differ per layer leave no empty blocks behind (a (k_max/64, Hkv, L)
+  // grid spent 8% of the EpiCache compaction on blocks that exit at once).
+  const int u = blockIdx.x;
+  int l = 0, hi = P.L;  // invariant: unit_off[l] <= u < unit_off[hi]
+  while (hi - l > 1) {
+    const int mid = (l + hi) >> 1;
+    if (P.unit_off[mid] <= u) l = mid; else hi = mid;
+  }
   const int k = P.k[l];
-  const int t0 = blockIdx.x * ROWS_PER_BLOCK;
-  if (t0 >= k) return;
+  const int tiles = (k + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
+  const int r = u - P.unit_off[l];
+  const int h = r / tiles;
+  const int t0 = (r - h * tiles) * ROWS_PER_BLOCK;
   const int64_t lh = static_cast<int64_t>(l) * P.Hkv + h;
   const int32_t* id = idx + P.idx_off[l] + static_cast<int64_t>(h) * k;
   const int64_t dst_base = (P.dst_ld >= 0) ? lh * P.dst_ld : P.dst_off[l] + static_cast<int64_t>(h) * k;
@@ -90,14 +100,21 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const uint4* __restrict
 
 cudaError_t launch_compact(const void* K, const void* V, const int32_t* idx, const int32_t* pos_src,
                            int32_t* pos_dst, void* Kc, void* Vc, const CompactParams& cp, cudaStream_t st) {
-  int kmax = 0;
-  for (int l = 0; l < cp.L; ++l)
-    if (cp.active[l] && cp.k[l] > kmax) kmax = cp.k[l];
-  if (kmax == 0) return cudaSuccess;
-  dim3 grid((kmax + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK, cp.Hkv, cp.L);
+  CompactParams p = cp;
+  int64_t units = 0;
+  for (int l = 0; l < p.L; ++l) {
+    p.unit_off[l] = static_cast<int32_t>(units);
+    if (p.active[l] && p.k[l] > 0) {
+      units += static_cast<int64_t>(p.Hkv) * ((p.k[l] + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK);
+    }
+  }
+  if (units > 0x7fffffff) return cudaErrorInvalidValue;
+  p.unit_off[p.L] = static_cast<int32_t>(units);
+  if (units == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(units));
   ProfScope ps("compact", st);
   compact_kernel<<<grid, THREADS, 0, st>>>(static_cast<const uint4*>(K), static_cast<const uint4*>(V), idx, pos_src,
-                                           pos_dst, static_cast<uint4*>(Kc), static_cast<uint4*>(Vc), cp,
+                                           pos_dst, static_cast<uint4*>(Kc), static_cast<uint4*>(Vc), p,
                                            status_word());
   return cudaGetLastError();
 }

@@ -115,6 +115,7 @@ struct CompactParams {
   int64_t idx_off[kMaxLayers];    // offset of layer l in the index array
   int64_t dst_off[kMaxLayers];    // ragged destination offset (rows) of layer l
   int32_t active[kMaxLayers];
+  int32_t unit_off[kMaxLayers + 1];  // filled by launch_compact: first (head, 64-row tile) unit of layer l
 };
 cudaError_t launch_compact(const void* K, const void* V, const int32_t* idx, const int32_t* pos_src,
                            int32_t* pos_dst, void* Kc, void* Vc, const CompactParams& cp, cudaStream_t st);
