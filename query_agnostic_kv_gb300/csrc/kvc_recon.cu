@@ -34,6 +34,7 @@
 // A gather kernel fills it (and the appended keys) from the query pool.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -171,6 +172,7 @@ struct KParams {
   int32_t CR, Rpad;                   // row-space chunk stride and rows per (l, h)
   int32_t ldApp;                      // appended-key rows per (l, h)
   int32_t units1;                     // pass-1 units per (l, h)
+  int32_t snake;                      // pass 1: odd rounds in reverse CTA order
   int n_units;
   float scale_log2;                   // log2(e) / sqrt(d)
   __nv_bfloat16* lsx;                 // [rows][16]: -lse2/scale_log2 in three bf16 terms
@@ -254,6 +256,20 @@ __device__ __forceinline__ int nq_of(const KParams& P, int ai, int r) {
 }
 
 // ----------------------------------------------------------------- units
+// The unit a CTA takes in round k, or -1 when it has none left (a round that
+// runs past n_units is the last one).  Pass-1 units differ in length when the
+// active layers do (EpiCache budgets); then the host lists the longest layers
+// first and sets P.snake, and odd rounds go to the CTAs in reverse, so the
+// CTAs that took the longest units in round 0 take the shortest ones in
+// round 1.
+template <int PASS>
+__device__ __forceinline__ int unit_of_round(const KParams& P, int k) {
+  const int c = (PASS == 1 && P.snake && (k & 1)) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                                                       : static_cast<int>(blockIdx.x);
+  const int u = k * static_cast<int>(gridDim.x) + c;
+  return u < P.n_units ? u : -1;
+}
+
 struct Unit {
   int ai, layer, h, lh, slab, n;
   int ntile;       // A tiles present (1..NA)
@@ -576,7 +592,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         y = static_cast<int32_t>(W.lh * P.ldK + W.key0 + t * TILE_ROWS);
         return W.slab ? &tmK1 : &tmK0;
       };
-      for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
+      for (int k = 0, u; (u = unit_of_round<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
         const Unit U = decode_unit<PASS>(P, u);
         if (!mbar_wait(&bars->a_empty[ab], aph ^ 1, P.limit_ns)) { fail(); break; }
         mbar_arrive_expect_tx(&bars->a_full[ab], U.ntile * TILE_BYTES);
@@ -589,8 +605,9 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         }
         ++loads_a;
         auto prefetch_next = [&]() {
-          if (u + static_cast<int>(gridDim.x) >= P.n_units) return;
-          const Unit W = decode_unit<PASS>(P, u + gridDim.x);
+          const int un = unit_of_round<PASS>(P, k + 1);
+          if (un < 0) return;
+          const Unit W = decode_unit<PASS>(P, un);
           for (int t = 0; t < W.ntile; ++t) {
             int32_t y;
             const CUtensorMap* map = a_tile(W, t, y);
@@ -641,7 +658,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
       int s = 0, ab = 0, db = 0;
       uint32_t bph = 0, aph = 0, dph = 0;
-      for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
+      for (int k = 0, u; (u = unit_of_round<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
         const Unit U = decode_unit<PASS>(P, u);
         if (!mbar_wait(&bars->a_full[ab], aph, P.limit_ns)) { fail(); break; }
         tc_fence_after();
@@ -697,7 +714,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
     int db = 0;
     uint32_t dph = 0;
     uint32_t comb_ph = 0;  // pass 1: phase of the per-unit half-row hand-off
-    for (int u = blockIdx.x; u < P.n_units && !*abort_flag; u += gridDim.x) {
+    for (int k = 0, u; (u = unit_of_round<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
       const Unit U = decode_unit<PASS>(P, u);
       const bool has_tile = wg < U.ntile;
       if (PASS == 1) {
@@ -1044,9 +1061,19 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   memset(&kp, 0, sizeof(kp));
   kp.Hkv = pr.Hkv; kp.Hq = pr.Hq; kp.G = G; kp.sinks = pr.sinks; kp.n_active = pr.n_active;
   constexpr int span2 = Cfg<2>::NA * TILE_ROWS;
+  // Schedule order of the active layers: longest first (stable), so that the
+  // pass-1 rounds pair long units with short ones (see unit_of_round).  Every
+  // buffer is addressed by model layer, so the order changes no result.
+  int ord[kMaxLayers];
+  for (int a = 0; a < pr.n_active; ++a) ord[a] = a;
+#ifndef KVC_SORT_LAYERS
+#define KVC_SORT_LAYERS 1
+#endif
+  if (KVC_SORT_LAYERS)
+    std::stable_sort(ord, ord + pr.n_active, [&](int x, int y) { return pr.lay[x].n > pr.lay[y].n; });
   int acc = 0;
   for (int a = 0; a < pr.n_active; ++a) {
-    const ReconLayer& ly = pr.lay[a];
+    const ReconLayer& ly = pr.lay[ord[a]];
     kp.layer[a] = ly.layer; kp.n[a] = ly.n; kp.m[a] = ly.m; kp.n_chunks[a] = ly.n_chunks;
     kp.last_len[a] = ly.last_len; kp.slab[a] = ly.slab;
     kp.unit_off[a] = acc;
@@ -1054,6 +1081,8 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
     acc += pr.Hkv * ((ly.n_chunks - 1) * pf + pl);
   }
   kp.unit_off[pr.n_active] = acc;
+  for (int a = 1; a < pr.n_active; ++a)
+    if (pr.lay[a].n != pr.lay[0].n) kp.snake = 1;
   kp.ldK = pr.ldK;
   kp.nq_full = pr.nq_full; kp.nq_last = pr.nq_last; kp.Q = pr.Q;
   kp.CR = CR; kp.Rpad = Rpad;
