@@ -417,10 +417,19 @@ def test_bounds_status_path(qk):
     assert qk.kvc_stream_status() == 4
 
 
-def test_block_prefill_matches_oracle(qk):
+EPI_CASES = {
+    "epi-small": dict(L=3, Hkv=2, Hq=6, mean_budget=300),
+    # 20 x 8 over-budget heads at the last blocks: 160 row-LSE units of
+    # different lengths on 152 SMs, so the second, reversed round is taken
+    "epi-20x8": dict(L=20, Hkv=8, Hq=24, mean_budget=600),
+}
+
+
+@pytest.mark.parametrize("name", list(EPI_CASES))
+def test_block_prefill_matches_oracle(qk, name):
     """EpiCache-style streaming with per-layer budgets, small shapes."""
-    cfg = ks.EpiConfig("epi-small", L=3, Hkv=2, Hq=6, d=128, n_hist=1500, block=256, episodes=1, prompt_len=24,
-                       mean_budget=300, alpha=3.0, sinks=4)
+    cfg = ks.EpiConfig(name, d=128, n_hist=1500, block=256, episodes=1, prompt_len=24, alpha=3.0, sinks=4,
+                       **EPI_CASES[name])
     sens = ks.gen_sensitivity(cfg)
     budgets = qk.kvc_layer_budgets(sens.tolist(), cfg.alpha, cfg.mean_budget, cfg.sinks)
     assert budgets == kv2.layer_budgets(sens.astype(np.float64), cfg.alpha, cfg.mean_budget, cfg.sinks).tolist()
@@ -442,21 +451,27 @@ def test_block_prefill_matches_oracle(qk):
         vb = to_dev(np.ascontiguousarray(Vh[:, :, t0:t1]))
         qk.kvc_block_prefill_step(st, kb, vb, t1 - t0, Qp_d, Kp_d, P, ws=ws)
         assert qk.kvc_stream_status() == 0
+    Kst_all = [bits_of(slabs[0]).reshape(L, H, cap, 128), bits_of(slabs[2]).reshape(L, H, cap, 128)]
+    pst_all = [pos[0].cpu().numpy().reshape(L, H, cap), pos[1].cpu().numpy().reshape(L, H, cap)]
+    same = total = 0
     for l in range(L):
         ref = kv2.block_prefill_layer(kv2.bf16_to_f64(Kh[l]), kv2.bf16_to_f64(Vh[l]), kv2.bf16_to_f64(Qp[l]),
                                       kv2.bf16_to_f64(Kp[l]), B, budgets[l], cfg.sinks)
         n = st.len[l]
         assert n == ref[0].shape[1]
         c = st.cur[l]
-        Kst = bits_of(slabs[2 * c]).reshape(L, H, cap, 128)
-        pst = pos[c].cpu().numpy().reshape(L, H, cap)
+        Kst, pst = Kst_all[c], pst_all[c]
         for h in range(H):
             got = pst[l, h, :n]
             assert np.all(np.diff(got) > 0) and set(range(cfg.sinks)) <= set(got.tolist())
             np.testing.assert_array_equal(Kst[l, h, :n], Kh[l, h][got])
-            # near-ties aside the kept global positions agree with the oracle
-            agree = len(set(got.tolist()) & set(ref[2][h].tolist())) / n
-            assert agree > 0.995, (l, h, agree)
+            # near-ties aside the kept global positions agree with the oracle:
+            # at most one swapped pair per head, 99.5% over all heads
+            g, r = set(got.tolist()), set(ref[2][h].tolist())
+            assert len(g ^ r) <= 2, (l, h, sorted(g - r), sorted(r - g))
+            same += len(g & r)
+            total += n
+    assert same / total > 0.995, same / total
 
 
 @pytest.mark.slow
