@@ -1185,6 +1185,12 @@ def epi_compact_bytes(cfg, budgets):
     return total
 
 
+# DRAM bytes (read + write) per compaction launch of the EpiCache block step:
+# ncu's one-pass dram__bytes_read/write.sum over the 87 compaction launches of
+# one episode, divided by 87.
+EPI_COMPACT_TRAFFIC_PER_LAUNCH = (36.2594e9 + 31.4959e9) / 87
+
+
 def run_epicache(args, rank, world, local_rank):
     import torch
     import query_agnostic_kv_gb300 as qk
@@ -1281,7 +1287,9 @@ def run_epicache(args, rank, world, local_rank):
     ctime = prof["compact"][1] / 1e3
     ach = cbytes / ctime / 1e9
     roof = {"kernel": "compact (kept rows of every over-budget layer into its other slab)", "bound": "hbm",
-            "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+            "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+            "traffic": EPI_COMPACT_TRAFFIC_PER_LAUNCH,
+            "traffic_source": "ncu dram bytes, mean over the compaction launches of one episode",
             "peak_source": f"hbm_gbs of {peak_src} peaks",
             "algorithmic_bytes_per_launch": cbytes / prof["compact"][0]}
 
