@@ -172,7 +172,7 @@ struct KParams {
   int32_t CR, Rpad;                   // row-space chunk stride and rows per (l, h)
   int32_t ldApp;                      // appended-key rows per (l, h)
   int32_t units1;                     // pass-1 units per (l, h)
-  int32_t snake;                      // pass 1: odd rounds in reverse CTA order
+  int32_t snake;                      // pass 1: odd waves in reverse CTA order
   int n_units;
   float scale_log2;                   // log2(e) / sqrt(d)
   __nv_bfloat16* lsx;                 // [rows][16]: -lse2/scale_log2 in three bf16 terms
@@ -256,14 +256,14 @@ __device__ __forceinline__ int nq_of(const KParams& P, int ai, int r) {
 }
 
 // ----------------------------------------------------------------- units
-// The unit a CTA takes in round k, or -1 when it has none left (a round that
-// runs past n_units is the last one).  Pass-1 units differ in length when the
-// active layers do (EpiCache budgets); then the host lists the longest layers
-// first and sets P.snake, and odd rounds go to the CTAs in reverse, so the
-// CTAs that took the longest units in round 0 take the shortest ones in
-// round 1.
+// The unit a CTA takes in wave k (units k*gridDim.x ... (k+1)*gridDim.x - 1),
+// or -1 when it has none left (a wave that runs past n_units is the last
+// one).  Pass-1 units differ in length when the active layers do (EpiCache
+// budgets); then the host lists the longest layers first and sets P.snake,
+// and odd waves go to the CTAs in reverse, so the CTAs that took the longest
+// units in the first wave take the shortest ones in the second.
 template <int PASS>
-__device__ __forceinline__ int unit_of_round(const KParams& P, int k) {
+__device__ __forceinline__ int unit_of_wave(const KParams& P, int k) {
   const int c = (PASS == 1 && P.snake && (k & 1)) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
                                                        : static_cast<int>(blockIdx.x);
   const int u = k * static_cast<int>(gridDim.x) + c;
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         y = static_cast<int32_t>(W.lh * P.ldK + W.key0 + t * TILE_ROWS);
         return W.slab ? &tmK1 : &tmK0;
       };
-      for (int k = 0, u; (u = unit_of_round<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
+      for (int k = 0, u; (u = unit_of_wave<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
         const Unit U = decode_unit<PASS>(P, u);
         if (!mbar_wait(&bars->a_empty[ab], aph ^ 1, P.limit_ns)) { fail(); break; }
         mbar_arrive_expect_tx(&bars->a_full[ab], U.ntile * TILE_BYTES);
@@ -605,7 +605,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         }
         ++loads_a;
         auto prefetch_next = [&]() {
-          const int un = unit_of_round<PASS>(P, k + 1);
+          const int un = unit_of_wave<PASS>(P, k + 1);
           if (un < 0) return;
           const Unit W = decode_unit<PASS>(P, un);
           for (int t = 0; t < W.ntile; ++t) {
@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
       int s = 0, ab = 0, db = 0;
       uint32_t bph = 0, aph = 0, dph = 0;
-      for (int k = 0, u; (u = unit_of_round<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
+      for (int k = 0, u; (u = unit_of_wave<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
         const Unit U = decode_unit<PASS>(P, u);
         if (!mbar_wait(&bars->a_full[ab], aph, P.limit_ns)) { fail(); break; }
         tc_fence_after();
@@ -714,7 +714,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
     int db = 0;
     uint32_t dph = 0;
     uint32_t comb_ph = 0;  // pass 1: phase of the per-unit half-row hand-off
-    for (int k = 0, u; (u = unit_of_round<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
+    for (int k = 0, u; (u = unit_of_wave<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
       const Unit U = decode_unit<PASS>(P, u);
       const bool has_tile = wg < U.ntile;
       if (PASS == 1) {
@@ -1062,7 +1062,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   kp.Hkv = pr.Hkv; kp.Hq = pr.Hq; kp.G = G; kp.sinks = pr.sinks; kp.n_active = pr.n_active;
   constexpr int span2 = Cfg<2>::NA * TILE_ROWS;
   // Schedule order of the active layers: longest first (stable), so that the
-  // pass-1 rounds pair long units with short ones (see unit_of_round).  Every
+  // pass-1 waves pair long units with short ones (see unit_of_wave).  Every
   // buffer is addressed by model layer, so the order changes no result.
   int ord[kMaxLayers];
   for (int a = 0; a < pr.n_active; ++a) ord[a] = a;

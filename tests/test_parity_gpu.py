@@ -420,7 +420,7 @@ def test_bounds_status_path(qk):
 EPI_CASES = {
     "epi-small": dict(L=3, Hkv=2, Hq=6, mean_budget=300),
     # 20 x 8 over-budget heads at the last blocks: 160 row-LSE units of
-    # different lengths on 152 SMs, so the second, reversed round is taken
+    # different lengths on 152 SMs, so the second, reversed wave is taken
     "epi-20x8": dict(L=20, Hkv=8, Hq=24, mean_budget=600),
 }
 
