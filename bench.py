@@ -368,7 +368,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         traffic = LSE_TRAFFIC_PER_LAYER * cfg.L
     roof = {"kernel": "recon_lse (tcgen05 row-LSE pass)", "bound": "tensor", "achieved": ach_lse,
             "peak": peak_tf, "unit": "TFLOP/s", "frac": ach_lse / peak_tf, "traffic": traffic,
-            "traffic_source": "ncu dram bytes of the 4-layer case, scaled by layers",
+            "traffic_source": "ncu dram bytes of the 4-layer case, scaled by layers; taken before the kernel "
+                              "gained its longest-first wave order, which applies only when the active layers "
+                              "differ in length (all layers are equally long here, so the loads are unchanged)",
             "peak_source": f"bf16_tflops_sustained of {peak_src} peaks",
             "algorithmic_flops_per_launch": work["flops_lse_per_launch"]}
     hbm = peaks.get("hbm_gbs")
