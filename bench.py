@@ -90,6 +90,8 @@ def algorithmic_work(cfg):
         "evict_topk": L * Hkv * N * 4 + L * Hkv * k * 4,
         "compact": 2 * 2 * L * Hkv * k * d * 2,     # read + write kept K and V
     }
+    # eviction and compaction fused into one launch
+    b["evict_compact"] = b["evict_topk"] + b["compact"]
     return {"flops_lse": f_lse * cfg.passes, "flops_colmax": f_col * cfg.passes, "Q": Q, "k": k,
             "bytes": b, "flops_lse_per_launch": f_lse, "flops_colmax_per_launch": f_col}
 
@@ -253,8 +255,11 @@ def run_reference(args, cfg, rank, world):
     for _ in range(args.warmup):
         time_oracle_sample(cfg, budget_s=0.0, sampler=smp)
     desc = ""
+    timed = []
     for _ in range(args.steps):
+        t0 = time.perf_counter()
         full, desc = time_oracle_sample(cfg, budget_s=0.0, sampler=smp)
+        timed.append(time.perf_counter() - t0)
         sample.append(full)
     t = statistics.median(sample)
     value = cfg.N / t
@@ -266,6 +271,10 @@ def run_reference(args, cfg, rank, world):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
                          "sample": "per step: " + desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        # each step times a bounded sample of the workload and scales it to
+        # the full step: ms_per_step and value are extrapolated, not timed
+        "extrapolated": True,
+        "timed_s_per_step": statistics.median(timed),
     }
     print(json.dumps(line), flush=True)
 
@@ -360,7 +369,11 @@ def run_ours(args, cfg, rank, world, local_rank):
                for n, v in prof.items()}
     lse_avg_s = prof["recon_lse"][1] / prof["recon_lse"][0] / 1e3
     col_avg_s = prof["recon_colmax"][1] / prof["recon_colmax"][0] / 1e3
-    peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    # The timed region is a short burst (well under a second of tensor work
+    # at the clocks sampled), so the burst bf16 peak is the denominator; the
+    # ratio to the power-capped sustained peak is reported beside it.
+    peak_tf = peaks.get("bf16_tflops")
+    peak_sus = peaks.get("bf16_tflops_sustained", peak_tf)
     ach_lse = work["flops_lse_per_launch"] / lse_avg_s / 1e12
     ach_col = work["flops_colmax_per_launch"] / col_avg_s / 1e12
     traffic = None
@@ -371,8 +384,10 @@ def run_ours(args, cfg, rank, world, local_rank):
             "traffic_source": "ncu dram bytes of the 4-layer case, scaled by layers; taken before the kernel "
                               "gained its longest-first wave order, which applies only when the active layers "
                               "differ in length (all layers are equally long here, so the loads are unchanged)",
-            "peak_source": f"bf16_tflops_sustained of {peak_src} peaks",
-            "algorithmic_flops_per_launch": work["flops_lse_per_launch"]}
+            "peak_source": f"bf16_tflops (burst) of {peak_src} peaks",
+            "frac_of_sustained": ach_lse / peak_sus,
+            "algorithmic_flops_per_launch": work["flops_lse_per_launch"],
+            "colmax": {"achieved": ach_col, "frac": ach_col / peak_tf}}
     hbm = peaks.get("hbm_gbs")
     bw = {}
     for name, b in work["bytes"].items():
@@ -383,8 +398,10 @@ def run_ours(args, cfg, rank, world, local_rank):
     f_all = work["flops_lse"] + work["flops_colmax"]
     b_all = sum(work["bytes"].values())
     t_roof = max(f_all / (peak_tf * 1e12), b_all / (hbm * 1e9))
+    t_roof_sus = max(f_all / (peak_sus * 1e12), b_all / (hbm * 1e9))
     step_roof = {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_per_step / 1e3),
-                 "tokens_per_s_at_roof": N / t_roof}
+                 "tokens_per_s_at_roof": N / t_roof, "peak": "bf16_tflops (burst) and hbm_gbs",
+                 "frac_of_sustained": t_roof_sus / (ms_per_step / 1e3)}
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -510,8 +527,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                     if i + 1 < n:
                         prep_back(i + 1)
                     stream.wait_event(ev_out[b])                 # host copies of step i-2 are done
-                    qk.kvc_evict_topk(shape, scoreb[b], S, kl, kept2[b], ws=wsb[b], stream=stream)
-                    qk.kvc_compact(shape, Kbuf[b], hV, kept2[b], kl, Kc2[b], Vc2[b], stream=stream)
+                    qk.kvc_evict_compact(shape, scoreb[b], S, kl, kept2[b], Kbuf[b], hV, Kc2[b], Vc2[b], ws=wsb[b],
+                                         stream=stream)
                     ev_done[b].record(stream)
                     if i + 2 < n:
                         copy_k(i + 2, [ev_gath[(i + 1) % 2], ev_done[b]])
@@ -566,7 +583,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         full, desc = time_oracle_sample(cfg, budget_s=20.0)
         cpu = {"value": N / full, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": desc,
-               "extrapolated_s_per_step": full}
+               "extrapolated": True, "extrapolated_s_per_step": full}
 
     graph = None
     if args.graph:
