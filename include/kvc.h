@@ -139,9 +139,20 @@ KVC_API size_t kvc_workspace_size(kvc_shape shape, int32_t sinks, int32_t m, dou
  *   K      device bf16 [L][Hkv][N][d]
  *   p      device f32 [N]                          (output)
  *   s_opt  device f32 [L][Hkv][N] or NULL          (output)
- *   ws     workspace of kvc_workspace_size() bytes */
+ *   ws     device workspace, 256-byte aligned, of at least
+ *          kvc_proxy_workspace_size(shape, s_opt == NULL) bytes (or
+ *          kvc_workspace_size() bytes, which covers it); it holds the
+ *          per-head scores when s_opt is NULL and may be NULL otherwise.
+ *          Too small or misaligned: KVC_ERR_WORKSPACE.
+ * The result is deterministic: the mean key of a head is summed in a fixed
+ * order. */
 KVC_API kvc_status kvc_proxy_score(kvc_shape shape, const void* K, float* p, float* s_opt, void* ws, size_t ws_bytes,
                            kvc_stream stream);
+
+/* Bytes of workspace kvc_proxy_score needs for this shape, with room for the
+ * per-head scores when with_scores is nonzero (s_opt NULL).  0 on invalid
+ * shapes. */
+KVC_API size_t kvc_proxy_workspace_size(kvc_shape shape, int32_t with_scores);
 
 /* Stage-1 proxy kinds.  KV² page, "어떻게 동작하나": KeyDiff is the default;
  * "전제와 한계": Knorm is the close alternative.  Knorm here scores
@@ -156,18 +167,20 @@ KVC_API kvc_status kvc_proxy_score_kind(kvc_shape shape, kvc_proxy_kind kind, co
 
 /* The pages have no counterpart to this entry point.  Same result as
  * kvc_proxy_score (p only) for callers that cannot allocate device memory
- * when they need the proxy -- runtimes that give all free HBM to their own
+ * at the point of the call: runtimes that hand all free HBM to their own
  * pool allocator, or hot paths that must not call cudaMalloc because it can
- * synchronise the device.  The per-head scratch lives in a 16 MiB array
- * inside the library, reserved on each GPU the first time the library's
- * module is loaded there and held until the process exits; this call
- * allocates nothing.  Limit: L*Hkv*N <= 4194304 (e.g. 32 layers x 8 KV
- * heads x 16384 tokens); larger shapes return KVC_ERR_WORKSPACE before any
- * launch.  The first call on a device looks up the array's device address
- * (once per device, with that device current); make that first call before
- * any stream capture.  All calls on a device share the array: calls that
- * may overlap on the GPU race and must be ordered by the caller.  No part of
- * the array needs clearing between calls.
+ * synchronise the device.  The scratch (the per-head scores) lives in a
+ * 16 MiB array inside the library, reserved on each GPU the first time the
+ * library's module is loaded there and held until the process exits; this
+ * call allocates nothing.  Limit: kvc_proxy_workspace_size(shape, 1) <=
+ * 16 MiB, that is L*Hkv*N <= 4194304 (e.g. 32 layers x 8 KV heads x 16384
+ * tokens, exactly at the limit); larger shapes return KVC_ERR_WORKSPACE
+ * before any launch.  The first call on a device (and the first after a
+ * cudaDeviceReset) looks up the array's device address with that device
+ * current; make that first call before any stream capture.  All calls on a
+ * device share the array: calls that may overlap on the GPU race and must
+ * be ordered by the caller.  No part of the array needs clearing between
+ * calls: every call overwrites all the entries it reads.
  *   K  device bf16 [L][Hkv][N][d];  p  device f32 [N] (output) */
 KVC_API kvc_status kvc_proxy_score_noalloc(kvc_shape shape, const void* K, float* p, kvc_stream stream);
 
@@ -244,6 +257,15 @@ KVC_API kvc_status kvc_evict_topk(kvc_shape shape, float* score, int32_t sinks, 
  *   Kc, Vc       device bf16 ragged (output); V/Vc may be NULL together */
 KVC_API kvc_status kvc_compact(kvc_shape shape, const void* K, const void* V, const int32_t* kept,
                        const int32_t* k_per_layer, void* Kc, void* Vc, kvc_stream stream);
+
+/* kvc_evict_topk followed by kvc_compact, in one launch: each (layer, KV
+ * head) copies its kept K/V rows into the compacted cache as soon as it has
+ * chosen them (the same results as the two calls; one kernel ramp instead
+ * of two).  Arguments, layouts and errors as in those two calls; ws needs
+ * at least 256 bytes, 256-byte aligned. */
+KVC_API kvc_status kvc_evict_compact(kvc_shape shape, float* score, int32_t sinks, const int32_t* k_per_layer,
+                                     int32_t* kept, const void* K, const void* V, void* Kc, void* Vc, void* ws,
+                                     size_t ws_bytes, kvc_stream stream);
 
 /* Whole KV² compression: proxy, then `passes` rounds of query selection and
  * reconstruction scoring (each round's mean score replacing the proxy),

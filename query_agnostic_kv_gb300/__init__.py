@@ -21,9 +21,9 @@ __all__ = [
     "KVCError", "kvc_shape", "kvc_block_state", "lib", "shape_of",
     "kvc_status_string", "kvc_device_check", "kvc_stream_status", "kvc_set_wait_limit_ns",
     "kvc_debug_expire_wait", "kvc_chunk_plan", "kvc_budget_count", "kvc_workspace_size",
-    "kvc_proxy_score", "kvc_select_queries", "kvc_recon_score", "kvc_recon_gather", "kvc_recon_rows",
+    "kvc_proxy_score", "kvc_proxy_workspace_size", "kvc_select_queries", "kvc_recon_score", "kvc_recon_gather", "kvc_recon_rows",
     "kvc_recon_cols", "kvc_refine_proxy", "kvc_evict_topk",
-    "kvc_compact", "kvc_compress", "kvc_layer_budgets", "kvc_block_state_init",
+    "kvc_compact", "kvc_evict_compact", "kvc_compress", "kvc_layer_budgets", "kvc_block_state_init",
     "kvc_block_workspace_size", "kvc_block_prefill_step", "EXPORTED",
 ]
 
@@ -63,6 +63,7 @@ _SIGS = {
     "kvc_budget_count": (c_i32, [c_dbl, c_i32, c_i32, ctypes.POINTER(c_i32)]),
     "kvc_workspace_size": (c_sz, [kvc_shape, c_i32, c_i32, c_dbl]),
     "kvc_proxy_score": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_proxy_workspace_size": (c_sz, [kvc_shape, c_i32]),
     "kvc_select_queries": (c_i32, [c_i32, c_i32, c_i32, c_dbl, c_vp, c_vp, c_vp]),
     "kvc_recon_score": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_vp, c_vp, c_vp, c_vp, c_sz,
                                 c_vp]),
@@ -72,6 +73,8 @@ _SIGS = {
     "kvc_refine_proxy": (c_i32, [kvc_shape, c_vp, c_i32, c_vp, c_vp]),
     "kvc_evict_topk": (c_i32, [kvc_shape, c_vp, c_i32, ctypes.POINTER(c_i32), c_vp, c_vp, c_sz, c_vp]),
     "kvc_compact": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, ctypes.POINTER(c_i32), c_vp, c_vp, c_vp]),
+    "kvc_evict_compact": (c_i32, [kvc_shape, c_vp, c_i32, ctypes.POINTER(c_i32), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                  c_sz, c_vp]),
     "kvc_compress": (c_i32, [kvc_shape, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_i32, ctypes.POINTER(c_i32), c_vp,
                              c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "kvc_layer_budgets": (c_i32, [ctypes.POINTER(ctypes.c_float), c_i32, c_dbl, c_i64, c_i32,
@@ -143,8 +146,14 @@ def _shape(s) -> kvc_shape:
     return kvc_shape(L, Hkv, Hq, d, N)
 
 
-def _dev(t, dtype=None, name="tensor"):
-    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+def _numel_ok(t, numel, name):
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call reads or writes {numel}")
+
+
+def _dev(t, dtype=None, name="tensor", numel=None):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL) holding at
+    least `numel` elements when given."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
@@ -153,10 +162,11 @@ def _dev(t, dtype=None, name="tensor"):
         raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    _numel_ok(t, numel, name)
     return c_vp(t.data_ptr())
 
 
-def _dev_or_pinned(t, dtype=None, name="tensor"):
+def _dev_or_pinned(t, dtype=None, name="tensor", numel=None):
     """Like _dev, but also accepts a pinned (page-locked) host tensor, which
     is mapped into the device address space: kernels then read only the rows
     they need across the host link instead of a full copy."""
@@ -167,8 +177,28 @@ def _dev_or_pinned(t, dtype=None, name="tensor"):
             raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
+        _numel_ok(t, numel, name)
         return c_vp(t.data_ptr())
-    return _dev(t, dtype, name)
+    return _dev(t, dtype, name, numel)
+
+
+def _n(shape):
+    """Element counts the KV² calls touch for a shape: keys/values, query
+    pool, per-head scores, p."""
+    L, Hkv, Hq, d, N = (shape.L, shape.Hkv, shape.Hq, shape.d, shape.N) if isinstance(shape, kvc_shape) else shape
+    return {"K": L * Hkv * N * d, "Q": L * Hq * N * d, "S": L * Hkv * N, "N": N, "L": L, "Hkv": Hkv, "Hq": Hq,
+            "d": d}
+
+
+def _n_queries(N, sinks, m, rho):
+    """Reconstruction queries of the chunk plan (None for a plan the library
+    refuses; the call then reports it)."""
+    n = c_i32(0)
+    if lib().kvc_chunk_plan(N, sinks, m, float(rho), ctypes.byref(n), None) != 0:
+        return None
+    off = (c_i32 * (n.value + 1))()
+    lib().kvc_chunk_plan(N, sinks, m, float(rho), ctypes.byref(n), off)
+    return off[n.value]
 
 
 def _ws(ws):
@@ -252,11 +282,16 @@ def kvc_layer_budgets(sens: Sequence[float], alpha: float, mean_budget: int, sin
 
 
 # ---------------------------------------------------------------- KV² stages
+def kvc_proxy_workspace_size(shape, with_scores: bool = True) -> int:
+    return int(lib().kvc_proxy_workspace_size(_shape(shape), 1 if with_scores else 0))
+
+
 def kvc_proxy_score(shape, K, p, s=None, ws=None, stream=None) -> None:
     w, wb = _ws(ws)
-    _check("kvc_proxy_score", lib().kvc_proxy_score(_shape(shape), _dev(K, torch.bfloat16, "K"),
-                                                    _dev(p, torch.float32, "p"), _dev(s, torch.float32, "s"),
-                                                    w, wb, _stream(stream)))
+    n = _n(shape)
+    _check("kvc_proxy_score", lib().kvc_proxy_score(_shape(shape), _dev(K, torch.bfloat16, "K", n["K"]),
+                                                    _dev(p, torch.float32, "p", n["N"]),
+                                                    _dev(s, torch.float32, "s", n["S"]), w, wb, _stream(stream)))
 
 
 KVC_PROXY_KEYDIFF = 0
@@ -271,9 +306,10 @@ def _proxy_kind(kind) -> int:
 def kvc_proxy_score_kind(shape, kind, K, p, s=None, ws=None, stream=None) -> None:
     """kvc_proxy_score with a proxy kind: "keydiff" (default) or "knorm"."""
     w, wb = _ws(ws)
+    n = _n(shape)
     _check("kvc_proxy_score_kind", lib().kvc_proxy_score_kind(
-        _shape(shape), _proxy_kind(kind), _dev(K, torch.bfloat16, "K"), _dev(p, torch.float32, "p"),
-        _dev(s, torch.float32, "s"), w, wb, _stream(stream)))
+        _shape(shape), _proxy_kind(kind), _dev(K, torch.bfloat16, "K", n["K"]), _dev(p, torch.float32, "p", n["N"]),
+        _dev(s, torch.float32, "s", n["S"]), w, wb, _stream(stream)))
 
 
 def kvc_compress_ex(shape, proxy, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, Kc, Vc, p=None, sel=None,
@@ -287,34 +323,44 @@ def kvc_compress_ex(shape, proxy, K, V, Qpool, sinks, m, rho, passes, k_per_laye
         if not gather_done.cuda_event:
             raise ValueError("gather_done must be a created event (record it once first)")
         ev = c_vp(gather_done.cuda_event)
+    n = _n(shape)
+    nk = n["Hkv"] * sum(int(k) for k in k_per_layer)
+    nq = _n_queries(n["N"], sinks, m, rho)
     _check("kvc_compress_ex", lib().kvc_compress_ex(
-        _shape(shape), _proxy_kind(proxy), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(V, torch.bfloat16, "V"),
-        _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"), sinks, m, float(rho), passes, _i32_array(k_per_layer),
-        _dev(kept, torch.int32, "kept"), _dev(Kc, torch.bfloat16, "Kc"), _dev(Vc, torch.bfloat16, "Vc"),
-        _dev(p, torch.float32, "p"), _dev(sel, torch.int32, "sel"), _dev(score, torch.float32, "score"), w, wb,
-        _stream(stream), ev))
+        _shape(shape), _proxy_kind(proxy), _dev(K, torch.bfloat16, "K", n["K"]),
+        _dev_or_pinned(V, torch.bfloat16, "V", n["K"]), _dev_or_pinned(Qpool, torch.bfloat16, "Qpool", n["Q"]), sinks,
+        m, float(rho), passes, _i32_array(k_per_layer), _dev(kept, torch.int32, "kept", nk),
+        _dev(Kc, torch.bfloat16, "Kc", nk * n["d"]), _dev(Vc, torch.bfloat16, "Vc", nk * n["d"]),
+        _dev(p, torch.float32, "p", n["N"]), _dev(sel, torch.int32, "sel", nq), _dev(score, torch.float32, "score", n["S"]),
+        w, wb, _stream(stream), ev))
 
 
 def kvc_proxy_score_noalloc(shape, K, p, stream=None) -> None:
     """kvc_proxy_score without a workspace: for callers that cannot allocate
     device memory at this point (their runtime owns all free HBM, or the call
     sits on a path where cudaMalloc is not allowed).  Scratch comes from a
-    16 MiB array inside the library; L*Hkv*N must not exceed 4194304."""
+    16 MiB array inside the library; L*Hkv*N must not exceed 4194304 (32
+    layers x 8 KV heads x 16K tokens is exactly at the limit)."""
+    n = _n(shape)
     _check("kvc_proxy_score_noalloc", lib().kvc_proxy_score_noalloc(
-        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev(p, torch.float32, "p"), _stream(stream)))
+        _shape(shape), _dev(K, torch.bfloat16, "K", n["K"]), _dev(p, torch.float32, "p", n["N"]), _stream(stream)))
 
 
 def kvc_select_queries(N, sinks, m, rho, p, sel, stream=None) -> None:
-    _check("kvc_select_queries", lib().kvc_select_queries(N, sinks, m, float(rho), _dev(p, torch.float32, "p"),
-                                                          _dev(sel, torch.int32, "sel"), _stream(stream)))
+    _check("kvc_select_queries", lib().kvc_select_queries(N, sinks, m, float(rho), _dev(p, torch.float32, "p", N),
+                                                          _dev(sel, torch.int32, "sel", _n_queries(N, sinks, m, rho)),
+                                                          _stream(stream)))
 
 
 def kvc_recon_score(shape, K, Qpool, sel, sinks, m, rho, score, Kapp=None, lse=None, ws=None, stream=None) -> None:
     w, wb = _ws(ws)
+    n = _n(shape)
+    nq = _n_queries(n["N"], sinks, m, rho) or 0
     _check("kvc_recon_score", lib().kvc_recon_score(
-        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"),
-        _dev(sel, torch.int32, "sel"), sinks, m, float(rho), _dev(Kapp, torch.bfloat16, "Kapp"),
-        _dev(score, torch.float32, "score"), _dev(lse, torch.float32, "lse"), w, wb, _stream(stream)))
+        _shape(shape), _dev(K, torch.bfloat16, "K", n["K"]), _dev_or_pinned(Qpool, torch.bfloat16, "Qpool", n["Q"]),
+        _dev(sel, torch.int32, "sel", nq), sinks, m, float(rho),
+        _dev(Kapp, torch.bfloat16, "Kapp", n["L"] * n["Hkv"] * nq * n["d"]), _dev(score, torch.float32, "score", n["S"]),
+        _dev(lse, torch.float32, "lse", n["L"] * n["Hq"] * nq), w, wb, _stream(stream)))
 
 
 def kvc_recon_gather(shape, K, Qpool, sel, sinks, m, rho, Kapp=None, ws=None, stream=None) -> None:
@@ -343,33 +389,54 @@ def kvc_recon_cols(shape, K, sinks, m, rho, score, ws=None, stream=None) -> None
 
 
 def kvc_refine_proxy(shape, score, sinks, p, stream=None) -> None:
-    _check("kvc_refine_proxy", lib().kvc_refine_proxy(_shape(shape), _dev(score, torch.float32, "score"), sinks,
-                                                      _dev(p, torch.float32, "p"), _stream(stream)))
+    n = _n(shape)
+    _check("kvc_refine_proxy", lib().kvc_refine_proxy(_shape(shape), _dev(score, torch.float32, "score", n["S"]),
+                                                      sinks, _dev(p, torch.float32, "p", n["N"]), _stream(stream)))
 
 
 def kvc_evict_topk(shape, score, sinks, k_per_layer, kept, ws=None, stream=None) -> None:
     w, wb = _ws(ws)
-    _check("kvc_evict_topk", lib().kvc_evict_topk(_shape(shape), _dev(score, torch.float32, "score"), sinks,
-                                                  _i32_array(k_per_layer), _dev(kept, torch.int32, "kept"), w, wb,
+    n = _n(shape)
+    nk = n["Hkv"] * sum(int(k) for k in k_per_layer)
+    _check("kvc_evict_topk", lib().kvc_evict_topk(_shape(shape), _dev(score, torch.float32, "score", n["S"]), sinks,
+                                                  _i32_array(k_per_layer), _dev(kept, torch.int32, "kept", nk), w, wb,
                                                   _stream(stream)))
 
 
 def kvc_compact(shape, K, V, kept, k_per_layer, Kc, Vc, stream=None) -> None:
-    _check("kvc_compact", lib().kvc_compact(_shape(shape), _dev_or_pinned(K, torch.bfloat16, "K"),
-                                            _dev_or_pinned(V, torch.bfloat16, "V"), _dev(kept, torch.int32, "kept"),
-                                            _i32_array(k_per_layer), _dev(Kc, torch.bfloat16, "Kc"),
-                                            _dev(Vc, torch.bfloat16, "Vc"), _stream(stream)))
+    n = _n(shape)
+    nk = n["Hkv"] * sum(int(k) for k in k_per_layer)
+    _check("kvc_compact", lib().kvc_compact(_shape(shape), _dev_or_pinned(K, torch.bfloat16, "K", n["K"]),
+                                            _dev_or_pinned(V, torch.bfloat16, "V", n["K"]),
+                                            _dev(kept, torch.int32, "kept", nk), _i32_array(k_per_layer),
+                                            _dev(Kc, torch.bfloat16, "Kc", nk * n["d"]),
+                                            _dev(Vc, torch.bfloat16, "Vc", nk * n["d"]), _stream(stream)))
+
+
+def kvc_evict_compact(shape, score, sinks, k_per_layer, kept, K, V, Kc, Vc, ws=None, stream=None) -> None:
+    """kvc_evict_topk and kvc_compact in one launch."""
+    w, wb = _ws(ws)
+    n = _n(shape)
+    nk = n["Hkv"] * sum(int(k) for k in k_per_layer)
+    _check("kvc_evict_compact", lib().kvc_evict_compact(
+        _shape(shape), _dev(score, torch.float32, "score", n["S"]), sinks, _i32_array(k_per_layer),
+        _dev(kept, torch.int32, "kept", nk), _dev_or_pinned(K, torch.bfloat16, "K", n["K"]),
+        _dev_or_pinned(V, torch.bfloat16, "V", n["K"]), _dev(Kc, torch.bfloat16, "Kc", nk * n["d"]),
+        _dev(Vc, torch.bfloat16, "Vc", nk * n["d"]), w, wb, _stream(stream)))
 
 
 def kvc_compress(shape, K, V, Qpool, sinks, m, rho, passes, k_per_layer, kept, Kc, Vc, p=None, sel=None,
                  score=None, ws=None, stream=None) -> None:
     w, wb = _ws(ws)
+    n = _n(shape)
+    nk = n["Hkv"] * sum(int(k) for k in k_per_layer)
+    nq = _n_queries(n["N"], sinks, m, rho)
     _check("kvc_compress", lib().kvc_compress(
-        _shape(shape), _dev(K, torch.bfloat16, "K"), _dev_or_pinned(V, torch.bfloat16, "V"),
-        _dev_or_pinned(Qpool, torch.bfloat16, "Qpool"), sinks, m, float(rho), passes, _i32_array(k_per_layer),
-        _dev(kept, torch.int32, "kept"), _dev(Kc, torch.bfloat16, "Kc"), _dev(Vc, torch.bfloat16, "Vc"),
-        _dev(p, torch.float32, "p"), _dev(sel, torch.int32, "sel"), _dev(score, torch.float32, "score"), w, wb,
-        _stream(stream)))
+        _shape(shape), _dev(K, torch.bfloat16, "K", n["K"]), _dev_or_pinned(V, torch.bfloat16, "V", n["K"]),
+        _dev_or_pinned(Qpool, torch.bfloat16, "Qpool", n["Q"]), sinks, m, float(rho), passes, _i32_array(k_per_layer),
+        _dev(kept, torch.int32, "kept", nk), _dev(Kc, torch.bfloat16, "Kc", nk * n["d"]),
+        _dev(Vc, torch.bfloat16, "Vc", nk * n["d"]), _dev(p, torch.float32, "p", n["N"]),
+        _dev(sel, torch.int32, "sel", nq), _dev(score, torch.float32, "score", n["S"]), w, wb, _stream(stream)))
 
 
 # ---------------------------------------------------------------- decode attention

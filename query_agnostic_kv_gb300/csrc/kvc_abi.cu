@@ -22,7 +22,7 @@ __device__ int g_status_word;
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int* g_status_ptr[kMaxDevices];
+SymbolSlot g_status_slot[kMaxDevices];
 int g_sms[kMaxDevices];
 int g_cc_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 unsupported
 uint64_t g_limit_ns = 1000000000ull;
@@ -82,17 +82,60 @@ ProfScope::~ProfScope() {
   if (slot < static_cast<int>(g_prof.size())) cudaEventRecord(g_prof[slot].ev1, stream);
 }
 
-int* status_word() {
+namespace {
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Unique ID of the calling thread's current context (false when there is
+// none yet, or the driver lacks the query).
+bool context_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    cudaGetLastError();
+  });
+  if (!g_ctx_current || !g_ctx_id) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+}  // namespace
+
+void* symbol_address(const void* symbol, SymbolSlot* slots) {
   const int d = current_device();
   if (d < 0) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[d]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    g_status_ptr[d] = static_cast<int*>(p);
+  unsigned long long id = 0;
+  const bool have_id = context_id(&id);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (have_id && slots[d].ptr && slots[d].ctx == id) return slots[d].ptr;
   }
-  return g_status_ptr[d];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  // cudaGetSymbolAddress made the primary context current if it was not yet
+  unsigned long long id2 = 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (context_id(&id2)) {
+    slots[d].ctx = id2;
+    slots[d].ptr = p;
+  } else {
+    slots[d].ptr = nullptr;   // no context ID to key it by: look it up every time
+  }
+  return p;
 }
+
+int* status_word() { return static_cast<int*>(symbol_address(&g_status_word, g_status_slot)); }
 
 uint64_t wait_limit_ns() { return g_limit_ns; }
 
@@ -233,13 +276,21 @@ bool reachable(const T* p, const R*... rest) {
   return (p == nullptr || device_can_read(p)) && reachable(rest...);
 }
 
+}  // namespace
+
+namespace kvc {
 bool shape_ok(const kvc_shape& s) {
   if (s.L < 1 || s.L > kMaxLayers || s.Hkv < 1 || s.Hq < s.Hkv || s.Hq % s.Hkv != 0 || s.d != kHeadDim || s.N < 1)
     return false;
+  // (layer, KV head) pairs index a grid dimension of the proxy and eviction kernels
+  if (static_cast<int64_t>(s.L) * s.Hkv > 65535) return false;
   // row coordinates of TMA boxes are int32
   const int64_t rows = static_cast<int64_t>(s.L) * s.Hq * s.N;
   return rows < (int64_t(1) << 31);
 }
+}  // namespace kvc
+
+namespace {
 
 kvc_status device_ok() {
   const int d = current_device();
@@ -264,7 +315,8 @@ struct KV2Workspace {
   uint32_t* gmax = nullptr;
   float* p = nullptr;
   int32_t* sel = nullptr;
-  float* score = nullptr;  // also the per-head proxy scratch
+  float* score = nullptr;  // also the per-head proxy scores
+  void* pscratch = nullptr;  // KeyDiff work list and partial sums
   ReconWorkspace rw{};
   size_t bytes = 0;
   bool ok = false;
@@ -279,6 +331,7 @@ KV2Workspace carve_kv2(const kvc_shape& s, const ChunkPlan& plan, void* base, si
   w.p = c.take<float>(s.N);
   w.sel = c.take<int32_t>(plan.Q);
   w.score = c.take<float>(LH * s.N);
+  w.pscratch = c.take<uint8_t>(proxy_scratch_bytes(static_cast<int>(LH), s.N));
   w.rw.Rpad = recon_rows(G, plan.n_chunks, plan.nq_full, plan.nq_last);
   w.rw.Qg = c.take<uint16_t>(LH * w.rw.Rpad * kHeadDim);
   w.rw.Kg = c.take<uint16_t>(LH * plan.Q * kHeadDim);
@@ -337,7 +390,7 @@ kvc_status run_recon(const kvc_shape& s, const ChunkPlan& plan, int32_t sinks, c
 }
 
 kvc_status run_evict(const kvc_shape& s, float* score, int32_t sinks, const int32_t* k_per_layer, int32_t* kept,
-                     uint32_t* gmax, cudaStream_t st) {
+                     uint32_t* gmax, cudaStream_t st, const EvictCopy* copy = nullptr) {
   EvictParams ep;
   memset(&ep, 0, sizeof(ep));
   ep.L = s.L;
@@ -352,7 +405,7 @@ kvc_status run_evict(const kvc_shape& s, float* score, int32_t sinks, const int3
     ep.active[l] = 1;
     off += static_cast<int64_t>(s.Hkv) * k_per_layer[l];
   }
-  return cuda_status(launch_evict(score, ep, kept, gmax, true, st));
+  return cuda_status(launch_evict(score, ep, kept, gmax, true, copy, st));
 }
 
 kvc_status run_compact(const kvc_shape& s, const void* K, const void* V, const int32_t* kept,
@@ -491,6 +544,15 @@ size_t kvc_workspace_size(kvc_shape shape, int32_t sinks, int32_t m, double rho)
   return carve_kv2(shape, p, nullptr, 0).bytes;
 }
 
+size_t kvc_proxy_workspace_size(kvc_shape shape, int32_t with_scores) {
+  if (!shape_ok(shape)) return 0;
+  const int LH = shape.L * shape.Hkv;
+  Carver c(nullptr, 0);
+  if (with_scores) c.take<float>(static_cast<size_t>(LH) * shape.N);
+  c.take<uint8_t>(proxy_scratch_bytes(LH, shape.N));
+  return (c.used + 255) & ~size_t(255);
+}
+
 kvc_status kvc_proxy_score(kvc_shape shape, const void* K, float* p, float* s_opt, void* ws, size_t ws_bytes,
                            kvc_stream stream) {
   return kvc_proxy_score_kind(shape, KVC_PROXY_KEYDIFF, K, p, s_opt, ws, ws_bytes, stream);
@@ -501,18 +563,18 @@ kvc_status kvc_proxy_score_kind(kvc_shape shape, kvc_proxy_kind kind, const void
   if (!shape_ok(shape) || !K || !p || !aligned16(K) || (kind != KVC_PROXY_KEYDIFF && kind != KVC_PROXY_KNORM))
     return KVC_ERR_INVALID;
   if (!reachable(K, p, s_opt, ws)) return KVC_ERR_INVALID;
-  float* s = s_opt;
-  if (!s) {
-    // per-head scratch lives in the score region of the workspace
-    const size_t need = 256 + static_cast<size_t>(shape.L) * shape.Hkv * shape.N * sizeof(float);
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need) return KVC_ERR_WORKSPACE;
-    s = static_cast<float*>(ws);
-  }
+  // workspace: the per-head scores (when s_opt is NULL), then the KeyDiff
+  // scratch
+  const int LH = shape.L * shape.Hkv;
+  Carver c(ws, ws ? ws_bytes : 0);
+  float* s = s_opt ? s_opt : c.take<float>(static_cast<size_t>(LH) * shape.N);
+  void* scratch = kind == KVC_PROXY_KEYDIFF ? c.take<uint8_t>(proxy_scratch_bytes(LH, shape.N)) : nullptr;
+  const bool need_ws = !s_opt || (kind == KVC_PROXY_KEYDIFF && proxy_scratch_bytes(LH, shape.N) > 0);
+  if (need_ws && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || !c.ok)) return KVC_ERR_WORKSPACE;
   kvc_status d = device_ok();
   if (d != KVC_OK) return d;
-  const int LH = shape.L * shape.Hkv;
   return cuda_status(kind == KVC_PROXY_KNORM ? launch_knorm(K, LH, shape.N, s, p, cs(stream))
-                                             : launch_proxy(K, LH, shape.N, s, p, cs(stream)));
+                                             : launch_proxy(K, LH, shape.N, s, p, scratch, cs(stream)));
 }
 
 kvc_status kvc_select_queries(int32_t N, int32_t sinks, int32_t m, double rho, const float* p, int32_t* sel,
@@ -606,6 +668,28 @@ kvc_status kvc_evict_topk(kvc_shape shape, float* score, int32_t sinks, const in
   return run_evict(shape, score, sinks, k_per_layer, kept, static_cast<uint32_t*>(ws), cs(stream));
 }
 
+kvc_status kvc_evict_compact(kvc_shape shape, float* score, int32_t sinks, const int32_t* k_per_layer, int32_t* kept,
+                             const void* K, const void* V, void* Kc, void* Vc, void* ws, size_t ws_bytes,
+                             kvc_stream stream) {
+  if (!shape_ok(shape) || !score || !kept || !K || !Kc || sinks < 0 || sinks >= shape.N ||
+      (V == nullptr) != (Vc == nullptr) || !aligned16(K) || !aligned16(Kc) || (V && (!aligned16(V) || !aligned16(Vc))))
+    return KVC_ERR_INVALID;
+  if (!device_can_read(K) || (V && !device_can_read(V)) || !reachable(score, kept, Kc, Vc, ws)) return KVC_ERR_INVALID;
+  if (check_budgets(shape, sinks, k_per_layer) != KVC_OK) return KVC_ERR_INVALID;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < 256) return KVC_ERR_WORKSPACE;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  EvictCopy cp;
+  memset(&cp, 0, sizeof(cp));
+  cp.K[0] = K;
+  cp.V[0] = V;
+  cp.Kd[0] = Kc;
+  cp.Vd[0] = Vc;
+  cp.src_ld = shape.N;
+  cp.dst_ld = -1;
+  return run_evict(shape, score, sinks, k_per_layer, kept, static_cast<uint32_t*>(ws), cs(stream), &cp);
+}
+
 kvc_status kvc_compact(kvc_shape shape, const void* K, const void* V, const int32_t* kept,
                        const int32_t* k_per_layer, void* Kc, void* Vc, kvc_stream stream) {
   if (!shape_ok(shape) || !K || !kept || !Kc || (V == nullptr) != (Vc == nullptr) || !aligned16(K) ||
@@ -652,7 +736,7 @@ kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K,
   const int LH = shape.L * shape.Hkv;
   // stage 1: proxy (per-head scratch in the score buffer)
   const cudaError_t pe = (proxy == KVC_PROXY_KNORM) ? launch_knorm(K, LH, shape.N, score, p, st)
-                                                    : launch_proxy(K, LH, shape.N, score, p, st);
+                                                    : launch_proxy(K, LH, shape.N, score, p, w.pscratch, st);
   if (pe != cudaSuccess) return KVC_ERR_CUDA;
   for (int t = 0; t < passes; ++t) {
     if (launch_select(p, shape.N, sinks, plan, rho, sel, st) != cudaSuccess) return KVC_ERR_CUDA;
@@ -662,9 +746,17 @@ kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K,
     if (t + 1 < passes && launch_mean_heads(score, LH, shape.N, shape.N, sinks, p, st) != cudaSuccess)
       return KVC_ERR_CUDA;
   }
-  kvc_status r = run_evict(shape, score, sinks, k_per_layer, kept, w.gmax, st);
-  if (r != KVC_OK) return r;
-  return run_compact(shape, K, V, kept, k_per_layer, Kc, Vc, st);
+  // eviction and compaction in one launch: each (layer, KV head) copies its
+  // kept K/V rows into the compacted cache as soon as it has chosen them
+  EvictCopy cp;
+  memset(&cp, 0, sizeof(cp));
+  cp.K[0] = K;
+  cp.V[0] = V;
+  cp.Kd[0] = Kc;
+  cp.Vd[0] = Vc;
+  cp.src_ld = shape.N;
+  cp.dst_ld = -1;
+  return run_evict(shape, score, sinks, k_per_layer, kept, w.gmax, st, &cp);
 }
 
 kvc_status kvc_layer_budgets(const float* sens, int32_t L, double alpha, int64_t mean_budget, int32_t sinks,
@@ -860,30 +952,22 @@ kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk, const v
       ep.out_off[l] = static_cast<int64_t>(l) * Hkv * kmax;
       ep.active[l] = 1;
     }
-    if (launch_evict(w.score, ep, w.kept, nullptr, false, cst) != cudaSuccess) return KVC_ERR_CUDA;
-    // compaction moves each active layer into its other slab
+    // eviction and compaction in one launch: each active layer's kept rows
+    // (with their global positions) move into its other slab
+    EvictCopy cp;
+    memset(&cp, 0, sizeof(cp));
     for (int from = 0; from < 2; ++from) {
-      CompactParams cp;
-      memset(&cp, 0, sizeof(cp));
-      cp.L = L;
-      cp.Hkv = Hkv;
-      cp.src_ld = st->capacity;
-      cp.dst_ld = st->capacity;
-      bool any = false;
-      for (int a = 0; a < na; ++a) {
-        const int l = pr.lay[a].layer;
-        if (st->cur[l] != from) continue;
-        cp.n_src[l] = n_now[l];
-        cp.k[l] = st->budget[l];
-        cp.idx_off[l] = static_cast<int64_t>(l) * Hkv * kmax;
-        cp.active[l] = 1;
-        any = true;
-      }
-      if (!any) continue;
-      if (launch_compact(st->K[from], st->V[from], w.kept, st->pos[from], st->pos[1 - from], st->K[1 - from],
-                         st->V[1 - from], cp, cst) != cudaSuccess)
-        return KVC_ERR_CUDA;
+      cp.K[from] = st->K[from];
+      cp.V[from] = st->V[from];
+      cp.pos[from] = st->pos[from];
+      cp.Kd[from] = st->K[1 - from];
+      cp.Vd[from] = st->V[1 - from];
+      cp.posd[from] = st->pos[1 - from];
     }
+    cp.src_ld = st->capacity;
+    cp.dst_ld = st->capacity;
+    for (int l = 0; l < L; ++l) cp.slab[l] = st->cur[l];
+    if (launch_evict(w.score, ep, w.kept, nullptr, false, &cp, cst) != cudaSuccess) return KVC_ERR_CUDA;
   }
   // 3. host bookkeeping
   for (int l = 0; l < L; ++l) {

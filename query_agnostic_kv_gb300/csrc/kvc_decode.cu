@@ -44,21 +44,12 @@ constexpr int kTargetItems = 4864;           // work items aimed for (32 per SM)
 constexpr int kMinSplit = 512;               // keys
 constexpr int HDR_BYTES = 128;
 
-#ifndef KVC_DEC_NW
-#define KVC_DEC_NW 15
-#endif
-#ifndef KVC_DEC_NB
-#define KVC_DEC_NB 4
-#endif
-#ifndef KVC_DEC_STAGES
-#define KVC_DEC_STAGES 3
-#endif
 
 template <int GP>
 struct DCfg {
-  static constexpr int NW = GP <= 4 ? KVC_DEC_NW : 8;        // consumer warps
-  static constexpr int NB = GP <= 4 ? KVC_DEC_NB : 2;        // batches per warp per tile
-  static constexpr int STAGES = GP <= 4 ? KVC_DEC_STAGES : 6;
+  static constexpr int NW = GP <= 4 ? 15 : 8;        // consumer warps
+  static constexpr int NB = GP <= 4 ? 4 : 2;        // batches per warp per tile
+  static constexpr int STAGES = GP <= 4 ? 3 : 6;
   static constexpr int TK = KPW * NW * NB;                   // keys per stage
   static constexpr int TILE_BYTES = TK * ROW_BYTES;  // one of K or V
   static constexpr int QBYTES = GP * ROW_BYTES;      // the item's queries (first tile)

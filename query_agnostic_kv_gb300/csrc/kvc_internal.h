@@ -21,6 +21,23 @@ constexpr int kMaxLayers = KVC_MAX_LAYERS;
 bool is_device_memory(const void* p);
 bool device_can_read(const void* p);
 
+// Shape checks shared by every entry point that takes a kvc_shape: sizes
+// in range, d = 128, GQA divisibility, row coordinates within int32 and at
+// most 65535 (layer, KV head) pairs.
+bool shape_ok(const kvc_shape& s);
+
+// Device address of a __device__ symbol in the current device's current
+// context, cached per device under the context's unique ID.  A
+// cudaDeviceReset replaces the primary context and the module is loaded
+// again, possibly at another address; the next call then finds a new
+// context ID and looks the symbol up again instead of reusing a stale
+// address.  Null on failure.
+struct SymbolSlot {
+  unsigned long long ctx;
+  void* ptr;
+};
+void* symbol_address(const void* symbol, SymbolSlot* slots);  // slots: one per device (64)
+
 // Per-device status word (device address) and the process-wide wait limit.
 int* status_word();
 uint64_t wait_limit_ns();
@@ -79,7 +96,11 @@ bool make_tmap_rows16(CUtensorMap* map, const void* base, uint64_t rows, uint32_
 // Each returns cudaSuccess or the launch error.
 
 // KeyDiff proxy: s[lh][i] for LH = L*Hkv heads of N rows, then p = mean.
-cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, cudaStream_t st);
+// scratch: proxy_scratch_bytes(LH, N) bytes of device memory, 256-B aligned
+// (work-list counter, per-head arrivals and ready flags, partial sums, mean
+// keys); its control words are cleared on the stream before the launch.
+size_t proxy_scratch_bytes(int LH, int N);
+cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, void* scratch, cudaStream_t st);
 
 // Knorm proxy: s[lh][i] = -|k_i|, then p = mean.
 cudaError_t launch_knorm(const void* K, int LH, int N, float* s, float* p, cudaStream_t st);
@@ -102,8 +123,25 @@ struct EvictParams {
   int64_t out_off[kMaxLayers];    // output offset of layer l
   int32_t active[kMaxLayers];     // 0: layer skipped
 };
+// Copy of the kept rows made by the eviction kernel itself (optional): the
+// kept K/V rows of layer l (and their global positions, when pos arrays are
+// given) move from the source slab src[slab[l]] to dst[slab[l]].  Rows are
+// 256-byte bf16 rows; V (and its destination) may be null.
+struct EvictCopy {
+  const void* K[2];
+  const void* V[2];
+  const int32_t* pos[2];
+  void* Kd[2];
+  void* Vd[2];
+  int32_t* posd[2];
+  int64_t src_ld;                 // rows per (l, h) in a source slab
+  int64_t dst_ld;                 // rows per (l, h) in a destination; < 0: ragged at out_off[l] + h*k_l
+  int32_t slab[kMaxLayers];
+};
+// gmax_word: two zeroed words of device memory when pin is set (the max
+// order key, an arrival counter).  copy: null, or the fused compaction.
 cudaError_t launch_evict(float* score, const EvictParams& ep, int32_t* kept, uint32_t* gmax_word, bool pin,
-                         cudaStream_t st);
+                         const EvictCopy* copy, cudaStream_t st);
 
 // Compaction: dst row (l, h, t) = src row (l, h, idx[l][h][t]).
 struct CompactParams {

@@ -26,38 +26,22 @@ namespace cg = cooperative_groups;
 namespace kvc {
 namespace {
 
-#ifndef KVC_KD_CTAS
-#define KVC_KD_CTAS 2
-#endif
-#ifndef KVC_KD_CACHE
-#define KVC_KD_CACHE 256
-#endif
-#ifndef KVC_KD_REVERSE
-#define KVC_KD_REVERSE 1
-#endif
-#ifndef KVC_KD_CLUSTER
-#define KVC_KD_CLUSTER 8
-#endif
-// 8 CTAs per head, two resident per SM (measured faster than 16-CTA clusters).
-constexpr int CLUSTER = KVC_KD_CLUSTER;
+// 8 CTAs per head, two resident per SM (16K workload: 0.302 ms; clusters of
+// 16, 4 and 2 CTAs measured 0.36, 0.32 and 0.33 ms; one 1024-thread CTA per
+// SM 0.35 ms).
+constexpr int CLUSTER = 8;
 constexpr int THREADS = 512;
-constexpr int CTAS_PER_SM = KVC_KD_CTAS;  // two clusters' CTAs share an SM: one loads while the other waits
+constexpr int CTAS_PER_SM = 2;            // two clusters' CTAs share an SM: one loads while the other waits
 constexpr int HALVES = THREADS / 16;      // half-warps per CTA
-#ifndef KVC_KD_UNROLL
-#define KVC_KD_UNROLL 8
-#endif
-constexpr int UNROLL = KVC_KD_UNROLL;      // rows per half-warp in flight per step (64 KB per CTA at 8)
-constexpr int CACHE_ROWS = KVC_KD_CACHE;  // rows of the slice kept in shared memory for pass B
+constexpr int UNROLL = 8;                 // rows per half-warp in flight per step (64 KB per CTA)
+constexpr int CACHE_ROWS = 256;           // rows of the slice kept in shared memory for pass B
 // Pass B walks the slice backwards: the rows pass A loaded last are the
 // likeliest to still be in L2, and the first rows come from the cache.
-constexpr bool PASS_B_REVERSE = KVC_KD_REVERSE != 0;
+constexpr bool PASS_B_REVERSE = true;
 constexpr int SMEM_BYTES = CACHE_ROWS * 256 + HALVES * 128 * 4;
-#ifndef KVC_KD_PREFETCH
-#define KVC_KD_PREFETCH 1
-#endif
-// Steps ahead of the L2 prefetch of rows (0: none).  16K workload: none
-// 0.311 ms, one step 0.302, two 0.355, three 0.388 (registers spill).
-constexpr int KD_PREFETCH = KVC_KD_PREFETCH;
+// Steps ahead of the L2 prefetch of rows.  16K workload: none 0.311 ms, one
+// step 0.302, two 0.355, three 0.388 (registers spill).
+constexpr int KD_PREFETCH = 1;
 
 // ---------------------------------------------------------------------------
 // Per-row arithmetic of the KeyDiff kernel.  Channel products run on packed
@@ -294,13 +278,17 @@ __global__ void mean_heads_kernel(const float* __restrict__ x, int LH, int N, in
 
 }  // namespace
 
-cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, cudaStream_t st) {
+// The cluster kernel needs no scratch beyond s.
+size_t proxy_scratch_bytes(int LH, int N) {
+  (void)LH;
+  (void)N;
+  return 0;
+}
+
+cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, void* scratch, cudaStream_t st) {
+  (void)scratch;
   cudaError_t e = cudaFuncSetAttribute(keydiff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if (CLUSTER > 8) {
-    e = cudaFuncSetAttribute(keydiff_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   dim3 grid(CLUSTER, LH);
   {
     ProfScope ps("keydiff", st);

@@ -8,11 +8,12 @@
 // persistent skeleton (warp 0: TMA producer, warp 1: tcgen05.mma issuer and
 // TMEM owner, then 4 warps per A tile as consumers):
 //
-//   pass 1 (row LSE)    A = 4 tiles of 128 reconstruction-query rows, B =
-//                       streamed 128-key tiles of the cache, then the chunk's
+//   pass 1 (row LSE)    A = 2 tiles of 128 reconstruction-query rows, B =
+//                       streamed 256-key tiles of the cache, then the chunk's
 //                       appended keys under the causal mask.  Each consumer
-//                       thread owns one query row (one TMEM lane) and keeps an
-//                       online max / sum of 2^x: lse2 = max + log2(sum).
+//                       thread owns half of one query row's columns (one TMEM
+//                       lane) and keeps a sum of 2^x against a lazily moved
+//                       reference: lse2 = reference + log2(sum).
 //                       On GB300 the MUFU exp2 rate (32/clk/SM) equals the
 //                       MMA logit rate at d = 128, so 16 consumer warps (4
 //                       per SM sub-partition) keep the exponentials flowing
@@ -52,28 +53,20 @@ constexpr int MAX_KST = 4;
 // Per-pass shape of the pipeline.  B tiles of 256 rows (MMA N = 256) halve
 // the A-operand re-reads from shared memory per FLOP; with N = 128 the
 // shared-memory operand traffic, not the tensor core, caps the MMA rate.
-#ifndef KVC_P1_CSPLIT
-#define KVC_P1_CSPLIT 2
-#endif
+// Pass 1 (8 layers of the 16K workload): two 128-column consumer groups per
+// accumulator 1.27 ms, one 256-column group 1.42 ms; double-buffered
+// accumulators on 128-key tiles 1.44-1.46 ms; 32-column TMEM loads
+// 1.39-1.43 ms against 64-column loads.
 template <int PASS>
 struct Cfg;
-#ifndef KVC_P1_BN
-#define KVC_P1_BN 256
-#endif
-#ifndef KVC_P1_DBUF
-#define KVC_P1_DBUF 1
-#endif
-#ifndef KVC_P1_KST
-#define KVC_P1_KST 2
-#endif
 template <>
 struct Cfg<1> {
   static constexpr int NA = 2;          // A tiles (128 query rows each) per unit
   static constexpr int ABUF = 1;        // A buffers in shared memory
-  static constexpr int DBUF = KVC_P1_DBUF;  // accumulator buffers per A tile
-  static constexpr int BN = KVC_P1_BN;  // rows (keys) of a B tile = MMA N
-  static constexpr int CSPLIT = KVC_P1_CSPLIT;  // consumer warps sharing one TMEM lane quarter (column split)
-  static constexpr int KST = KVC_P1_KST;  // B-tile ring depth
+  static constexpr int DBUF = 1;        // accumulator buffers per A tile
+  static constexpr int BN = 256;        // rows (keys) of a B tile = MMA N
+  static constexpr int CSPLIT = 2;      // consumer warps sharing one TMEM lane quarter (column split)
+  static constexpr int KST = 2;         // B-tile ring depth
 };
 // Pass 2: two 128-key A tiles per unit against 256-query B tiles (MMA
 // N = 256, nine K steps: eight of d = 128, one for the lse), one consumer
@@ -86,52 +79,20 @@ struct Cfg<1> {
 // 128-query tiles with the key tiles copied into TMEM, loads of the next
 // column block issued before folding the current one, and the last query
 // tile of a chunk multiplied at its own (smaller) N.
-#ifndef KVC_P2_BN
-#define KVC_P2_BN 256
-#endif
-#ifndef KVC_P2_CSPLIT
-#define KVC_P2_CSPLIT 1
-#endif
-#ifndef KVC_P2_KST
-#define KVC_P2_KST 2
-#endif
 template <>
 struct Cfg<2> {
   static constexpr int NA = 2;
   static constexpr int ABUF = 1;
   static constexpr int DBUF = 1;
-  static constexpr int BN = KVC_P2_BN;
-  static constexpr int CSPLIT = KVC_P2_CSPLIT;
-  static constexpr int KST = KVC_P2_KST;
+  static constexpr int BN = 256;
+  static constexpr int CSPLIT = 1;
+  static constexpr int KST = 2;
 };
 // Pass 2 refills its single A buffer (the next unit's 128-key tiles, read
 // once from HBM) only after the unit's last MMA; the producer warms those
 // tiles in L2 once the unit's second B tile is on its way.
-#ifndef KVC_A_PREFETCH
-#define KVC_A_PREFETCH 1
-#endif
-constexpr bool A_PREFETCH = KVC_A_PREFETCH != 0;
-// Pass-2 consumer columns per TMEM load (32 lets two consumer groups share
-// an accumulator within the register file).
-#ifndef KVC_P2_BLK
-#define KVC_P2_BLK 64
-#endif
-constexpr int P2_BLK = KVC_P2_BLK;
-static_assert(P2_BLK == 32 || P2_BLK == 64, "pass-2 TMEM load width");
-// Pass-1 consumer columns per TMEM load (8 layers of the 16K workload: 64
-// columns 1.25 ms; 32 columns 1.39-1.43 ms, though they free registers).
-#ifndef KVC_P1_BLK
-#define KVC_P1_BLK 64
-#endif
-constexpr int P1_BLK = KVC_P1_BLK;
-static_assert(P1_BLK == 32 || P1_BLK == 64, "pass-1 TMEM load width");
-template <int W>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[W]) {
-  if constexpr (W == 32)
-    tmem_ld32(taddr, v);
-  else
-    tmem_ld64(taddr, v);
-}
+// Both passes' consumers read their accumulator in 64-column TMEM loads.
+constexpr int P_BLK = 64;
 template <int PASS>
 constexpr int kThreads = 64 + 128 * Cfg<PASS>::NA * Cfg<PASS>::CSPLIT;
 template <int PASS>
@@ -192,44 +153,6 @@ __device__ __forceinline__ float lg2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Software exp2 (Cody-Waite range reduction + minimax polynomial, the split
-// of exponentials between MUFU and the FMA pipe used by FlashAttention-4):
-// x = n + f with n = round(x) (via the 1.5 * 2^23 rounding constant),
-// f in [-0.5, 0.5], 2^f ~= C0 + f (C1 + f (C2 + f C3)) with max relative
-// error 7.5e-5 (coefficients from csrc/fit_exp2_poly.py), 2^n added to the
-// exponent bits; x is clamped at -125 so that 2^n * p stays a normal number
-// (terms that small are below fp32 resolution of the row sum).  On GB300 the
-// MUFU exp2 rate already matches the MMA, and moving 3/8 of the
-// exponentials here measured 13% slower, so EMU_PAIRS is 0.
-constexpr float EXP2_C0 = 0.9999280571937561f;
-constexpr float EXP2_C1 = 0.6932609677314758f;
-constexpr float EXP2_C2 = 0.2426111251115799f;
-constexpr float EXP2_C3 = 0.0551716685295105f;
-constexpr float ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23
-#ifndef KVC_EMU_PAIRS
-#define KVC_EMU_PAIRS 0
-#endif
-constexpr int EMU_PAIRS = KVC_EMU_PAIRS;                // column pairs (of 32 per 64-column half) on the FMA pipe
-
-__device__ __forceinline__ uint64_t exp2_poly2(float x0, float x1) {
-  x0 = fmaxf(x0, -125.0f);
-  x1 = fmaxf(x1, -125.0f);
-  const uint64_t x = pack2(x0, x1);
-  const uint64_t t = add2(x, pack2(ROUND_MAGIC, ROUND_MAGIC));    // magic + n, exact
-  const uint64_t n = add2(t, pack2(-ROUND_MAGIC, -ROUND_MAGIC));  // n as float
-  const uint64_t f = fma2(n, pack2(-1.0f, -1.0f), x);              // x - n
-  uint64_t p = fma2(pack2(EXP2_C3, EXP2_C3), f, pack2(EXP2_C2, EXP2_C2));
-  p = fma2(p, f, pack2(EXP2_C1, EXP2_C1));
-  p = fma2(p, f, pack2(EXP2_C0, EXP2_C0));
-  float p0, p1, t0, t1;
-  unpack2(p, p0, p1);
-  unpack2(t, t0, t1);
-  // the low mantissa bits of t hold n; shifted into the exponent field
-  const float r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
-  const float r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
-  return pack2(r0, r1);
 }
 
 // Row o of the lse rows: x = -lse2/scale as three bf16 terms (hi + mid + lo
@@ -392,52 +315,11 @@ struct __align__(8) Bars {
   int abort_flag;
 };
 
-// Online log-sum-exp update of one row over `N` fp32 logits (already in
-// registers) of which the first `lim` are visible.
-template <int N>
-__device__ __forceinline__ void lse_update(float (&v)[N], int lim, float c, float& mrun, float& ssum) {
-  if (lim <= 0) return;
-  if (lim < N) {
-#pragma unroll
-    for (int k = 0; k < N; ++k) v[k] = (k < lim) ? v[k] : -INFINITY;
-  }
-  // tile max: 8 independent chains, then a tree
-  float t[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    float a = v[q];
-#pragma unroll
-    for (int k = q + 8; k + 8 < N; k += 16) a = fmax3(a, v[k], v[k + 8]);
-    if ((N / 8) % 2 == 0) a = fmaxf(a, v[N - 8 + q]);
-    t[q] = a;
-  }
-  const float bm = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
-  const float mn = fmaxf(mrun, bm * c);
-  ssum *= ex2(mrun - mn);  // 0 while nothing has been seen (mrun = -inf)
-  mrun = mn;
-  // sum of 2^(v*c - max): packed fp32 FMA/ADD, 4 packed partial sums
-  const uint64_t cc = pack2(c, c), nm = pack2(-mn, -mn);
-  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-  for (int k = 0; k < N / 2; ++k) {
-    float x0, x1;
-    unpack2(fma2(pack2(v[2 * k], v[2 * k + 1]), cc, nm), x0, x1);
-    const uint64_t e = (k < EMU_PAIRS) ? exp2_poly2(x0, x1) : pack2(ex2(x0), ex2(x1));
-    acc[k & 3] = add2(acc[k & 3], e);
-  }
-  const uint64_t s2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-  float s0, s1;
-  unpack2(s2, s0, s1);
-  ssum += s0 + s1;
-}
-
-#ifndef KVC_SUM_CHAINS
-#define KVC_SUM_CHAINS 8
-#endif
-// Sum of 2^(v*c - m) over N logits (masked entries are -inf and add 0).
+// Sum of 2^(v*c - m) over N logits (masked entries are -inf and add 0),
+// in eight packed partial sums (measured 1.1% faster than four).
 template <int N>
 __device__ __forceinline__ float exp2_sum(const float (&v)[N], float c, float m) {
-  constexpr int CH = KVC_SUM_CHAINS;                    // independent packed partial sums
+  constexpr int CH = 8;                                 // independent packed partial sums
   const uint64_t cc = pack2(c, c), nm = pack2(-m, -m);
   uint64_t acc[CH];
 #pragma unroll
@@ -446,8 +328,7 @@ __device__ __forceinline__ float exp2_sum(const float (&v)[N], float c, float m)
   for (int k = 0; k < N / 2; ++k) {
     float x0, x1;
     unpack2(fma2(pack2(v[2 * k], v[2 * k + 1]), cc, nm), x0, x1);
-    const uint64_t e = (k < EMU_PAIRS) ? exp2_poly2(x0, x1) : pack2(ex2(x0), ex2(x1));
-    acc[k % CH] = add2(acc[k % CH], e);
+    acc[k % CH] = add2(acc[k % CH], pack2(ex2(x0), ex2(x1)));
   }
 #pragma unroll
   for (int w = CH / 2; w >= 1; w /= 2)
@@ -498,16 +379,6 @@ __device__ __forceinline__ void lse_update_lazy(float (&v)[N], int lim, float c,
   ssum += s;
 }
 
-#ifndef KVC_LAZY_MAX
-#define KVC_LAZY_MAX 1
-#endif
-template <int N>
-__device__ __forceinline__ void row_update(float (&v)[N], int lim, float c, float& m, float& s) {
-  if (KVC_LAZY_MAX)
-    lse_update_lazy<N>(v, lim, c, m, s);
-  else
-    lse_update<N>(v, lim, c, m, s);
-}
 
 template <int PASS>
 __global__ void __launch_bounds__(kThreads<PASS>, 1)
@@ -642,7 +513,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
           tma_load_2d(dst + BHALF, map, 64, y, &bars->b_full[s]);
           ++loads_b;
-          if (PASS == 2 && A_PREFETCH && i == min(1, U.nT - 1)) prefetch_next();
+          if (PASS == 2 && i == min(1, U.nT - 1)) prefetch_next();
           if (++s == KST) { s = 0; bph ^= 1; }
         }
       }
@@ -729,7 +600,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         const int j = valid ? local - g * nq : 0;
         float mrun = -INFINITY, ssum = 0.f;
         constexpr int COLS = BN / CSPLIT;  // columns of the tile this warp reads
-        constexpr int PB = P1_BLK;         // columns per TMEM load
+        constexpr int PB = P_BLK;          // columns per TMEM load
         static_assert(COLS % PB == 0, "consumers read whole column blocks");
         for (int i = 0; i < U.nT; ++i) {
           uint64_t* df = &bars->d_full[db * NA + wg];
@@ -745,13 +616,13 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           for (int blk = 0; blk < COLS / PB; ++blk) {
             float v[PB];
             __syncwarp();
-            tmem_ld_cols(col + blk * PB, v);
+            tmem_ld64(col + blk * PB, v);
             if (blk == COLS / PB - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&bars->d_empty[db * NA + wg]);
             }
-            row_update<PB>(v, lim - blk * PB, c, mrun, ssum);
+            lse_update_lazy<PB>(v, lim - blk * PB, c, mrun, ssum);
           }
           if (++db == DBUF) { db = 0; dph ^= 1; }
         }
@@ -794,7 +665,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         // ---- column max over the chunk's queries: one key (TMEM lane) per
         // thread, this group's half of the accumulator's query columns
         constexpr int COLS = BN / CSPLIT;
-        constexpr int PB = P2_BLK;                       // columns per TMEM load
+        constexpr int PB = P_BLK;                        // columns per TMEM load
         static_assert(COLS % PB == 0, "pass-2 consumers read whole column blocks");
         const int pos = U.key0 + wg * TILE_ROWS + row;
         const bool valid = has_tile && pos < U.hi;
@@ -824,7 +695,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
           for (int blk = 0; blk < COLS / PB; ++blk) {
             float v[PB];
             __syncwarp();
-            tmem_ld_cols(col + blk * PB, v);
+            tmem_ld64(col + blk * PB, v);
             if (blk == COLS / PB - 1) {
               // the accumulator goes back to the MMA warp once it is in registers
               tc_fence_before();
@@ -1066,11 +937,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   // buffer is addressed by model layer, so the order changes no result.
   int ord[kMaxLayers];
   for (int a = 0; a < pr.n_active; ++a) ord[a] = a;
-#ifndef KVC_SORT_LAYERS
-#define KVC_SORT_LAYERS 1
-#endif
-  if (KVC_SORT_LAYERS)
-    std::stable_sort(ord, ord + pr.n_active, [&](int x, int y) { return pr.lay[x].n > pr.lay[y].n; });
+  std::stable_sort(ord, ord + pr.n_active, [&](int x, int y) { return pr.lay[x].n > pr.lay[y].n; });
   int acc = 0;
   for (int a = 0; a < pr.n_active; ++a) {
     const ReconLayer& ly = pr.lay[ord[a]];

@@ -5,8 +5,8 @@ the proxy -- a runtime that has handed all free HBM to its own pool, or a
 latency-critical path where cudaMalloc (which can synchronise the device)
 is not allowed.  It must give the same p as kvc_proxy_score, which takes its
 scratch from a caller-allocated workspace, on consecutive calls that reuse
-the library's built-in scratch, and must refuse shapes larger than that
-scratch before launching anything.
+the library's built-in scratch, also for a shape exactly at that scratch's
+size, and must refuse larger shapes before launching anything.
 
 This file is named so that pytest collects it last; it needs no state from
 the other test files.
@@ -56,10 +56,38 @@ def test_noalloc_matches_workspace_entry_point_twice(qk):
                               what="noalloc proxy p")
 
 
+LIMIT = 16 << 20   # bytes of the library's built-in scratch
+
+
+def _full_size_inputs(shape, seed):
+    L, H, _, d, N = shape
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    K = torch.randn(L * H * N * d, generator=g, device=DEV).to(torch.bfloat16)
+    p = torch.full((N,), float("nan"), dtype=torch.float32, device=DEV)
+    return K, p
+
+
+def test_noalloc_at_its_limit_matches_workspace_entry_point(qk):
+    # 32 x 8 heads of 16384 rows: L*Hkv*N = 4194304, exactly at the limit
+    shape = (32, 8, 32, 128, 16384)
+    need = qk.kvc_proxy_workspace_size(shape, True)
+    assert need == LIMIT
+    K, p = _full_size_inputs(shape, 3)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    p_ref = torch.empty_like(p)
+    qk.kvc_proxy_score(shape, K, p_ref, ws=ws)
+    qk.kvc_proxy_score_noalloc(shape, K, p)
+    assert qk.kvc_stream_status() == 0
+    compare.assert_scores(p.cpu().numpy(), p_ref.cpu().numpy(), floor=compare.PROXY_FLOOR, what="noalloc p at limit")
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch(qk):
-    shape = (32, 8, 32, 128, 16385)      # 32*8*16385 > 4194304
-    K = torch.empty(16, dtype=torch.bfloat16, device=DEV)
-    p = torch.empty(16, dtype=torch.float32, device=DEV)
+    shape = (32, 8, 32, 128, 16385)      # one row past the 16 MiB scratch
+    assert qk.kvc_proxy_workspace_size(shape, True) > LIMIT
+    # inputs at full size, so that nothing could read past them even if the
+    # host-side check were missing
+    K, p = _full_size_inputs(shape, 4)
     with pytest.raises(qk.KVCError) as e:
         qk.kvc_proxy_score_noalloc(shape, K, p)
     assert e.value.code == 5  # KVC_ERR_WORKSPACE, raised on the host before any launch
+    assert torch.isnan(p).all()          # nothing was written
