@@ -368,6 +368,34 @@ def test_compress_single_pass_equals_passes_one():
     assert len(out3["sel"]) == 3 and out3["sel"][0].tolist() == sel.tolist()
 
 
+def test_refinement_passes_follow_planted_needles():
+    """KV² page, "무엇과 다른가" (refinement): each pass's scores replace the
+    proxy for the next pass's selection.  Hand-built case with one chunk
+    [1, 6) and one reconstruction query per pass (rho = 0.2):
+      pass 1: KeyDiff ranks key 2 first -- it is the only key pointing against
+              the mean unit key (-e1 against five keys near +e1);
+      pass 2: the pool query at 2 is 100 e5, whose only nonzero logit is with
+              key 4 (0.1 e5 component), so key 4 takes most of the attention
+              and the refined proxy selects 4;
+      pass 3: the pool query at 4 is 100 e3, a needle on key 1 -> selects 1.
+    A dropped refinement (p kept), a refined p taken from the wrong pass or a
+    selection of the lowest instead of the highest scores changes this
+    sequence."""
+    d, N = 8, 6
+    e = np.eye(d)
+    K = np.stack([e[0], e[0] + 0.1 * e[2], -e[0], e[0] + 0.1 * e[3], e[0] + 0.1 * e[4], e[0] + 0.1 * e[5]])
+    Qp = np.zeros((N, d))
+    Qp[2] = 100 * e[4]
+    Qp[4] = 100 * e[2]
+    K4 = K[None, None]                  # [L=1][Hkv=1][N][d]
+    Q4 = Qp[None, None]                 # [L=1][Hq=1][N][d]
+    out = kv2.kv2_compress(K4, K4.copy(), Q4, 1, 5, 0.2, [2], passes=3)
+    assert [s.tolist() for s in out["sel"]] == [[2], [4], [1]]
+    # the last pass scores with the all-zero query at 1: every logit is 0, the
+    # attention is uniform, so the tie rule keeps the lowest non-sink position
+    assert out["kept"][0].tolist() == [[0, 1]]
+
+
 # ---------------------------------------------------------------------------
 # EpiCache: layer budgets and block prefill
 # ---------------------------------------------------------------------------
