@@ -52,10 +52,11 @@ def parse():
     ap.add_argument("--proxy", choices=["keydiff", "knorm"], default="keydiff", help="stage-1 proxy")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the step captured in a CUDA graph (launch-bound small workloads)")
-    ap.add_argument("--op", choices=["compress", "decode", "episode", "q4", "epicache"], default="compress",
+    ap.add_argument("--op", choices=["compress", "decode", "episode", "q4", "epicache", "rho"], default="compress",
                     help="compress: the KV² compression step; decode: attention over the compacted cache; "
                          "episode: EpiCache per-turn match + episode cache swap; q4: Q4 codec of the cache; "
-                         "epicache: EpiCache block prefill of every episode")
+                         "epicache: EpiCache block prefill of every episode; rho: the compression step at "
+                         "several reconstruction ratios")
     ap.add_argument("--decode-config", default=ks.DECODE_128K.name, choices=list(ks.DECODE_CONFIGS))
     return ap.parse_args()
 
@@ -1184,10 +1185,11 @@ def epi_oracle_sample(cfg):
                f"{cfg.n_hist} tokens")
 
 
-def epi_compact_bytes(cfg, budgets):
-    """Algorithmic bytes of the block step's compactions over one episode: an
-    over-budget layer moves its k_l kept K and V rows (read + write) and
-    their int32 positions, per KV head."""
+def epi_evict_compact_bytes(cfg, budgets):
+    """Algorithmic bytes of the block step's eviction + compaction launches
+    over one episode: an over-budget layer reads the n scores of each KV head,
+    writes its k_l kept indices, and moves the k_l kept K and V rows (read +
+    write) with their int32 positions."""
     B, S = cfg.block, cfg.sinks
     nb = (cfg.n_hist + B - 1) // B
     length = [0] * cfg.L
@@ -1197,17 +1199,16 @@ def epi_compact_bytes(cfg, budgets):
         for l in range(cfg.L):
             n = length[l] + blk
             if n > budgets[l] and n > S:
-                total += cfg.Hkv * budgets[l] * (2 * 2 * 128 * 2 + 2 * 4)
+                total += cfg.Hkv * (n * 4 + budgets[l] * 4 + budgets[l] * (2 * 2 * 128 * 2 + 2 * 4))
                 length[l] = budgets[l]
             else:
                 length[l] = n
     return total
 
 
-# DRAM bytes (read + write) per compaction launch of the EpiCache block step:
-# ncu's one-pass dram__bytes_read/write.sum over the 87 compaction launches of
-# one episode, divided by 87.
-EPI_COMPACT_TRAFFIC_PER_LAUNCH = (36.2594e9 + 31.4959e9) / 87
+# DRAM bytes (read + write) per eviction + compaction launch of the EpiCache
+# block step, from ncu; None until captured for the fused kernel.
+EPI_EVICT_TRAFFIC_PER_LAUNCH = None
 
 
 def run_epicache(args, rank, world, local_rank):
@@ -1253,6 +1254,8 @@ def run_epicache(args, rank, world, local_rank):
         dk = torch.from_numpy(np.stack([p[1] for p in prm]).view(np.int16)).view(torch.bfloat16).to(dev)
         prompts.append((dq, dk))
     cap = max(budgets) + B
+    torch.cuda.synchronize()
+    mem0 = torch.cuda.memory_allocated(dev)
     slabs = [torch.zeros(L * H * cap * 128, dtype=torch.bfloat16, device=dev) for _ in range(4)]
     pos = [torch.zeros(L * H * cap, dtype=torch.int32, device=dev) for _ in range(2)]
     stream = torch.cuda.current_stream()
@@ -1272,6 +1275,15 @@ def run_epicache(args, rank, world, local_rank):
 
     n_warm = max(3, args.warmup)
     ws = episode(0)
+    torch.cuda.synchronize()
+    memory = {
+        "block_state_and_workspace_bytes": torch.cuda.memory_allocated(dev) - mem0,
+        "workspace_bytes": ws.numel(),
+        "full_kv_cache_of_history_bytes": 2 * L * H * cfg.n_hist * 128 * 2,
+        "how": "device bytes allocated for the two K/V slabs, the position arrays and the step workspace (torch "
+               "allocator, measured), against the K and V of the whole history (computed from its shape); the "
+               "model weights and the history blocks themselves are not counted",
+    }
     for w in range(1, n_warm):
         episode(w % cfg.episodes, ws)
     torch.cuda.synchronize()
@@ -1299,18 +1311,18 @@ def run_epicache(args, rank, world, local_rank):
     total = sum(v[1] for v in prof.values())
     kernels = {n: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / total} for n, v in prof.items()}
 
-    # roofline of the dominant kernel: compaction, bound by HBM
+    # roofline of the eviction + compaction launch, bound by HBM
     peaks, peak_src = load_peaks()
     hbm = peaks.get("hbm_gbs")
-    cbytes = epi_compact_bytes(cfg, budgets) * cfg.episodes
-    ctime = prof["compact"][1] / 1e3
+    cbytes = epi_evict_compact_bytes(cfg, budgets) * cfg.episodes
+    ctime = prof["evict_compact"][1] / 1e3
     ach = cbytes / ctime / 1e9
-    roof = {"kernel": "compact (kept rows of every over-budget layer into its other slab)", "bound": "hbm",
+    roof = {"kernel": "evict_compact (top-M_l per KV head, kept rows into the other slab)", "bound": "hbm",
             "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-            "traffic": EPI_COMPACT_TRAFFIC_PER_LAUNCH,
-            "traffic_source": "ncu dram bytes, mean over the compaction launches of one episode",
+            "traffic": EPI_EVICT_TRAFFIC_PER_LAUNCH,
+            "traffic_source": "ncu dram bytes per launch (null: not captured for this kernel)",
             "peak_source": f"hbm_gbs of {peak_src} peaks",
-            "algorithmic_bytes_per_launch": cbytes / prof["compact"][0]}
+            "algorithmic_bytes_per_launch": cbytes / prof["evict_compact"][0]}
 
     # end to end: the history streamed from pinned host memory; block b is
     # copied on a copy stream into one of two device buffers while the step
@@ -1376,7 +1388,103 @@ def run_epicache(args, rank, world, local_rank):
                    "episodes": cfg.episodes, "prompt_queries": P, "mean_budget": cfg.mean_budget, "alpha": cfg.alpha,
                    "step": "one episode (all history blocks)", "l2": "history 10 GB on the device"},
         "roofline": roof, "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()), "clocks": clocks,
-        "e2e": e2e, "cpu_baseline": cpu}), flush=True)
+        "memory": memory, "e2e": e2e, "cpu_baseline": cpu}), flush=True)
+
+
+# ---------------------------------------------------------------- reconstruction-ratio sweep
+RHO_METRIC = "compression step time and workspace vs reconstruction ratio rho (Llama-8B shape, 16K)"
+RHO_SWEEP = (0.05, 0.1, 0.25, 0.5)
+
+
+def run_rho_sweep(args, rank, world, local_rank):
+    """KV² page, "무엇과 다른가": the method's runtime and peak activation
+    memory grow with the reconstruction ratio rho.  The 16K workload is
+    compressed at each rho of RHO_SWEEP (same cache, budget and sinks)."""
+    base = ks.LLAMA_16K
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        pts = []
+        for rho in RHO_SWEEP:
+            cfg = ks.scaled(base, rho=rho)
+            t, desc = time_oracle_sample(cfg, budget_s=2.0)
+            pts.append({"rho": rho, "ms_per_step": t * 1e3, "sample": desc})
+        v = base.N / (pts[1]["ms_per_step"] / 1e3)
+        print(json.dumps({"impl": "reference", "metric": RHO_METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+                          "steps": 1, "warmup": 0, "ms_per_step": pts[1]["ms_per_step"], "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": base.name + "-rho-sweep"}, "sweep": pts, "extrapolated": True,
+                          "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                                           "sample": "per rho: " + pts[1]["sample"]},
+                          "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    import torch
+    import query_agnostic_kv_gb300 as qk
+    from query_agnostic_kv_gb300 import _build
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _build.build_library()
+    qk.kvc_device_check()
+    x = ks.gen_kv2(base)
+    L, H, Hq, N, S, d = base.L, base.Hkv, base.Hq, base.N, base.sinks, base.d
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    K, V, Q = dev_bf16(x.K), dev_bf16(x.V), dev_bf16(x.Q)
+    shape = (L, H, Hq, d, N)
+    k = qk.kvc_budget_count(base.budget, N, S)
+    kept = torch.empty(L * H * k, dtype=torch.int32, device=dev)
+    Kc = torch.empty(L * H * k * d, dtype=torch.bfloat16, device=dev)
+    Vc = torch.empty_like(Kc)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+    pts = []
+    steps = max(1, min(args.steps, 50))
+    for rho in RHO_SWEEP:
+        cfg = ks.scaled(base, rho=rho)
+        work = algorithmic_work(cfg)
+        ws = torch.empty(qk.kvc_workspace_size(shape, S, cfg.m, rho), dtype=torch.uint8, device=dev)
+
+        def step():
+            qk.kvc_compress_ex(shape, "keydiff", K, V, Q, S, cfg.m, rho, 1, [k] * L, kept, Kc, Vc, ws=ws,
+                               stream=stream)
+
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        assert qk.kvc_stream_status(stream) == 0
+        qk.kvc_profile_begin()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        prof = qk.kvc_profile_end()
+        ms = a.elapsed_time(b) / steps
+        lse = prof["recon_lse"][1] / prof["recon_lse"][0]
+        col = prof["recon_colmax"][1] / prof["recon_colmax"][0]
+        f_step = work["flops_lse"] + work["flops_colmax"]
+        pts.append({"rho": rho, "ms_per_step": ms, "tokens_per_s": N / (ms / 1e3),
+                    "recon_lse_ms": lse, "recon_colmax_ms": col, "reconstruction_queries": work["Q"],
+                    "scoring_flops": f_step, "scoring_tflops": f_step / ((lse + col) / 1e3) / 1e12,
+                    "lse_frac_of_burst": work["flops_lse_per_launch"] / (lse / 1e3) / 1e12 / peaks["bf16_tflops"],
+                    "workspace_bytes": ws.numel()})
+        del ws
+        torch.cuda.empty_cache()
+    if rank == 0:
+        mid = pts[1]
+        print(json.dumps({
+            "metric": RHO_METRIC, "value": mid["tokens_per_s"], "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": max(3, args.warmup), "ms_per_step": mid["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": base.name + "-rho-sweep", "rho": list(RHO_SWEEP), "budget": base.budget,
+                       "m": base.m, "value_at_rho": 0.1}, "sweep": pts,
+            "peak_source": f"bf16_tflops of {peak_src} peaks"}), flush=True)
 
 
 def main():
@@ -1398,6 +1506,9 @@ def main():
         return
     if args.op == "epicache":
         run_epicache(args, rank, world, local_rank)
+        return
+    if args.op == "rho":
+        run_rho_sweep(args, rank, world, local_rank)
         return
     if args.impl == "reference":
         run_reference(args, cfg, rank, world)

@@ -165,6 +165,41 @@ typedef enum { KVC_PROXY_KEYDIFF = 0, KVC_PROXY_KNORM = 1 } kvc_proxy_kind;
 KVC_API kvc_status kvc_proxy_score_kind(kvc_shape shape, kvc_proxy_kind kind, const void* K, float* p, float* s_opt,
                                         void* ws, size_t ws_bytes, kvc_stream stream);
 
+/* Layer-sharded compression.  The KV² page's proxy is a mean over all
+ * (layer, KV head) pairs and its sink pin uses the max over all scores;
+ * everything else is per (layer, KV head).  A cache split by layers over
+ * several devices therefore exchanges only N floats per pass (a sum) and
+ * one float (a max).  Each shard calls these with the shape of its own
+ * layers (L = its layer count) and its slices of K, V, the query pool and
+ * the scores, which are contiguous in the [L][...] layouts:
+ *   kvc_proxy_partial    psum[i] = sum over the shard's heads of s_i (no
+ *                        division); s_opt/ws as in kvc_proxy_score
+ *   (caller: all-reduce(sum) of psum over the shards)
+ *   kvc_proxy_from_sums  p[i] = psum[i] / total_heads (L*Hkv of the whole
+ *                        cache): the proxy p of the unsharded call, up to
+ *                        the order of the additions
+ *   kvc_select_queries   on every shard (the same p gives the same queries)
+ *   kvc_recon_score      shard-local
+ *   kvc_refine_partial   (refinement passes) psum[i] = sum over the shard's
+ *                        heads of score[i], 0 for i < sinks; then the same
+ *                        all-reduce and kvc_proxy_from_sums
+ *   kvc_evict_compact    shard-local (pins the sinks to the shard's max,
+ *                        which changes no kept position)
+ *   kvc_score_max        *max_out (device f32) = the shard's largest
+ *                        non-sink score; ws: 256 bytes of device scratch
+ *   (caller: all-reduce(max))
+ *   kvc_pin_sinks        score[l][h][s] = *value (device f32) for s < sinks
+ * Device pointers throughout; psum, p: f32 [N]. */
+KVC_API kvc_status kvc_proxy_partial(kvc_shape shape, kvc_proxy_kind kind, const void* K, float* psum, float* s_opt,
+                                     void* ws, size_t ws_bytes, kvc_stream stream);
+KVC_API kvc_status kvc_refine_partial(kvc_shape shape, const float* score, int32_t sinks, float* psum,
+                                      kvc_stream stream);
+KVC_API kvc_status kvc_proxy_from_sums(int32_t N, int32_t total_heads, const float* psum, float* p,
+                                       kvc_stream stream);
+KVC_API kvc_status kvc_score_max(kvc_shape shape, const float* score, int32_t sinks, float* max_out, void* ws,
+                                 size_t ws_bytes, kvc_stream stream);
+KVC_API kvc_status kvc_pin_sinks(kvc_shape shape, float* score, int32_t sinks, const float* value, kvc_stream stream);
+
 /* The pages have no counterpart to this entry point.  Same result as
  * kvc_proxy_score (p only) for callers that cannot allocate device memory
  * at the point of the call: runtimes that hand all free HBM to their own
@@ -327,7 +362,12 @@ KVC_API kvc_status kvc_block_state_init(kvc_block_state* st, int32_t L, int32_t 
                                 void* V1, int32_t* pos1);
 
 /* Workspace bytes for kvc_block_prefill_step with blocks of up to
- * `max_block` tokens and P prompt queries. */
+ * `max_block` tokens and P prompt queries.  The workspace begins with the
+ * last step's scores, f32 [L][Hkv][capacity]: for every layer that step
+ * scored, row i of (l, h) holds the score of cache row i of the appended
+ * cache (its kept rows, then the block) for i in [sinks, len + blk_len); the
+ * rest of that region is unspecified.  Callers may read it for diagnostics
+ * until the next call that uses the workspace. */
 KVC_API size_t kvc_block_workspace_size(const kvc_block_state* st, int32_t max_block, int32_t P);
 
 /* "[26'ICML] EpiCache", "방법: 3단계" step ② and Fig. 1(b,c): append one

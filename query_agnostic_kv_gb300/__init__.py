@@ -23,7 +23,8 @@ __all__ = [
     "kvc_debug_expire_wait", "kvc_chunk_plan", "kvc_budget_count", "kvc_workspace_size",
     "kvc_proxy_score", "kvc_proxy_workspace_size", "kvc_select_queries", "kvc_recon_score", "kvc_recon_gather", "kvc_recon_rows",
     "kvc_recon_cols", "kvc_refine_proxy", "kvc_evict_topk",
-    "kvc_compact", "kvc_evict_compact", "kvc_compress", "kvc_layer_budgets", "kvc_block_state_init",
+    "kvc_compact", "kvc_evict_compact", "kvc_compress", "kvc_proxy_partial", "kvc_refine_partial",
+    "kvc_proxy_from_sums", "kvc_score_max", "kvc_pin_sinks", "kvc_layer_budgets", "kvc_block_state_init",
     "kvc_block_workspace_size", "kvc_block_prefill_step", "EXPORTED",
 ]
 
@@ -85,6 +86,11 @@ _SIGS = {
     "kvc_block_prefill_step": (c_i32, [ctypes.POINTER(kvc_block_state), c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_vp,
                                        c_sz, c_vp]),
     "kvc_proxy_score_noalloc": (c_i32, [kvc_shape, c_vp, c_vp, c_vp]),
+    "kvc_proxy_partial": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_refine_partial": (c_i32, [kvc_shape, c_vp, c_i32, c_vp, c_vp]),
+    "kvc_proxy_from_sums": (c_i32, [c_i32, c_i32, c_vp, c_vp, c_vp]),
+    "kvc_score_max": (c_i32, [kvc_shape, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
+    "kvc_pin_sinks": (c_i32, [kvc_shape, c_vp, c_i32, c_vp, c_vp]),
     "kvc_proxy_score_kind": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "kvc_compress_ex": (c_i32, [kvc_shape, c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_dbl, c_i32,
                                 ctypes.POINTER(c_i32), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
@@ -344,6 +350,43 @@ def kvc_proxy_score_noalloc(shape, K, p, stream=None) -> None:
     n = _n(shape)
     _check("kvc_proxy_score_noalloc", lib().kvc_proxy_score_noalloc(
         _shape(shape), _dev(K, torch.bfloat16, "K", n["K"]), _dev(p, torch.float32, "p", n["N"]), _stream(stream)))
+
+
+# ---------------------------------------------------------------- layer-sharded calls
+def kvc_proxy_partial(shape, kind, K, psum, s=None, ws=None, stream=None) -> None:
+    """psum[i] = sum over this shard's (layer, KV head) pairs of the proxy s_i."""
+    w, wb = _ws(ws)
+    n = _n(shape)
+    _check("kvc_proxy_partial", lib().kvc_proxy_partial(
+        _shape(shape), _proxy_kind(kind), _dev(K, torch.bfloat16, "K", n["K"]), _dev(psum, torch.float32, "psum", n["N"]),
+        _dev(s, torch.float32, "s", n["S"]), w, wb, _stream(stream)))
+
+
+def kvc_refine_partial(shape, score, sinks, psum, stream=None) -> None:
+    n = _n(shape)
+    _check("kvc_refine_partial", lib().kvc_refine_partial(
+        _shape(shape), _dev(score, torch.float32, "score", n["S"]), sinks, _dev(psum, torch.float32, "psum", n["N"]),
+        _stream(stream)))
+
+
+def kvc_proxy_from_sums(N, total_heads, psum, p, stream=None) -> None:
+    _check("kvc_proxy_from_sums", lib().kvc_proxy_from_sums(
+        N, total_heads, _dev(psum, torch.float32, "psum", N), _dev(p, torch.float32, "p", N), _stream(stream)))
+
+
+def kvc_score_max(shape, score, sinks, max_out, ws=None, stream=None) -> None:
+    w, wb = _ws(ws)
+    n = _n(shape)
+    _check("kvc_score_max", lib().kvc_score_max(
+        _shape(shape), _dev(score, torch.float32, "score", n["S"]), sinks, _dev(max_out, torch.float32, "max_out", 1),
+        w, wb, _stream(stream)))
+
+
+def kvc_pin_sinks(shape, score, sinks, value, stream=None) -> None:
+    n = _n(shape)
+    _check("kvc_pin_sinks", lib().kvc_pin_sinks(
+        _shape(shape), _dev(score, torch.float32, "score", n["S"]), sinks, _dev(value, torch.float32, "value", 1),
+        _stream(stream)))
 
 
 def kvc_select_queries(N, sinks, m, rho, p, sel, stream=None) -> None:

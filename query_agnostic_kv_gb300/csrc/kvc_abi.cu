@@ -577,6 +577,59 @@ kvc_status kvc_proxy_score_kind(kvc_shape shape, kvc_proxy_kind kind, const void
                                              : launch_proxy(K, LH, shape.N, s, p, scratch, cs(stream)));
 }
 
+kvc_status kvc_proxy_partial(kvc_shape shape, kvc_proxy_kind kind, const void* K, float* psum, float* s_opt,
+                             void* ws, size_t ws_bytes, kvc_stream stream) {
+  if (!shape_ok(shape) || !K || !psum || !aligned16(K) || (kind != KVC_PROXY_KEYDIFF && kind != KVC_PROXY_KNORM))
+    return KVC_ERR_INVALID;
+  if (!reachable(K, psum, s_opt, ws)) return KVC_ERR_INVALID;
+  const int LH = shape.L * shape.Hkv;
+  float* s = s_opt;
+  if (!s) {
+    const size_t need = static_cast<size_t>(LH) * shape.N * sizeof(float);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need) return KVC_ERR_WORKSPACE;
+    s = static_cast<float*>(ws);
+  }
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  const cudaError_t e = launch_proxy_scores(kind == KVC_PROXY_KNORM ? 1 : 0, K, LH, shape.N, s, cs(stream));
+  if (e != cudaSuccess) return KVC_ERR_CUDA;
+  return cuda_status(launch_sum_heads(s, LH, shape.N, shape.N, 0, psum, cs(stream)));
+}
+
+kvc_status kvc_refine_partial(kvc_shape shape, const float* score, int32_t sinks, float* psum, kvc_stream stream) {
+  if (!shape_ok(shape) || !score || !psum || sinks < 0 || sinks >= shape.N || !reachable(score, psum))
+    return KVC_ERR_INVALID;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return cuda_status(launch_sum_heads(score, shape.L * shape.Hkv, shape.N, shape.N, sinks, psum, cs(stream)));
+}
+
+kvc_status kvc_proxy_from_sums(int32_t N, int32_t total_heads, const float* psum, float* p, kvc_stream stream) {
+  if (N < 1 || total_heads < 1 || !psum || !p || !reachable(psum, p)) return KVC_ERR_INVALID;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return cuda_status(launch_sums_to_mean(psum, N, total_heads, p, cs(stream)));
+}
+
+kvc_status kvc_score_max(kvc_shape shape, const float* score, int32_t sinks, float* max_out, void* ws, size_t ws_bytes,
+                         kvc_stream stream) {
+  if (!shape_ok(shape) || !score || !max_out || sinks < 0 || sinks >= shape.N || !reachable(score, max_out, ws))
+    return KVC_ERR_INVALID;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < 256) return KVC_ERR_WORKSPACE;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return cuda_status(launch_score_max(score, shape.L * shape.Hkv, shape.N, sinks, static_cast<uint32_t*>(ws), max_out,
+                                      cs(stream)));
+}
+
+kvc_status kvc_pin_sinks(kvc_shape shape, float* score, int32_t sinks, const float* value, kvc_stream stream) {
+  if (!shape_ok(shape) || !score || !value || sinks < 0 || sinks >= shape.N || !reachable(score, value))
+    return KVC_ERR_INVALID;
+  kvc_status d = device_ok();
+  if (d != KVC_OK) return d;
+  return cuda_status(launch_pin_value(score, shape.L * shape.Hkv, shape.N, sinks, value, cs(stream)));
+}
+
 kvc_status kvc_select_queries(int32_t N, int32_t sinks, int32_t m, double rho, const float* p, int32_t* sel,
                               kvc_stream stream) {
   ChunkPlan plan;

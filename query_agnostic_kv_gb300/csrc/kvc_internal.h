@@ -108,6 +108,18 @@ cudaError_t launch_knorm(const void* K, int LH, int N, float* s, float* p, cudaS
 // p[i] = mean over LH rows of x[lh][i] (stride ld); p[i] = 0 for i < zero_below.
 cudaError_t launch_mean_heads(const float* x, int LH, int N, int64_t ld, int zero_below, float* p,
                               cudaStream_t st);
+// The same sum without the division (a shard's partial sum), and the
+// division of summed partials by the total head count.
+cudaError_t launch_sum_heads(const float* x, int LH, int N, int64_t ld, int zero_below, float* psum,
+                             cudaStream_t st);
+cudaError_t launch_sums_to_mean(const float* psum, int N, int heads, float* p, cudaStream_t st);
+// Per-head proxy scores only: kind 0 KeyDiff, 1 Knorm.
+cudaError_t launch_proxy_scores(int kind, const void* K, int LH, int N, float* s, cudaStream_t st);
+// Largest non-sink score of every (l, h) row into *max_out (device f32), and
+// score[l][h][s] = *value for s < sinks.
+cudaError_t launch_score_max(const float* score, int LH, int N, int sinks, uint32_t* key_word, float* max_out,
+                             cudaStream_t st);
+cudaError_t launch_pin_value(float* score, int LH, int N, int sinks, const float* value, cudaStream_t st);
 
 // Per-chunk selection of reconstruction queries.
 cudaError_t launch_select(const float* p, int N, int sinks, const ChunkPlan& plan, double rho, int32_t* sel,

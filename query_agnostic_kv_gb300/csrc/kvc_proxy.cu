@@ -262,8 +262,9 @@ __global__ void __launch_bounds__(256) knorm_kernel(const uint4* __restrict__ K,
   }
 }
 
-// p[i] = (1/LH) sum_h x[h][i] (fixed order), 0 below `zero_below`.
-__global__ void mean_heads_kernel(const float* __restrict__ x, int LH, int N, int64_t ld, int zero_below,
+// p[i] = (1/LH) sum_h x[h][i] (fixed order), 0 below `zero_below`; with
+// `divide` 0 the plain sum (a shard's partial sum for the layer-sharded path).
+__global__ void mean_heads_kernel(const float* __restrict__ x, int LH, int N, int64_t ld, int zero_below, int divide,
                                   float* __restrict__ p) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N) return;
@@ -273,7 +274,14 @@ __global__ void mean_heads_kernel(const float* __restrict__ x, int LH, int N, in
   }
   float t = 0.f;
   for (int h = 0; h < LH; ++h) t += x[static_cast<int64_t>(h) * ld + i];
-  p[i] = t / static_cast<float>(LH);
+  p[i] = divide ? t / static_cast<float>(LH) : t;
+}
+
+// p[i] = psum[i] / heads (the division of the unsharded mean, applied to the
+// shards' summed partials).
+__global__ void sums_to_mean_kernel(const float* __restrict__ psum, int N, int heads, float* __restrict__ p) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < N) p[i] = psum[i] / static_cast<float>(heads);
 }
 
 }  // namespace
@@ -316,7 +324,39 @@ cudaError_t launch_knorm(const void* K, int LH, int N, float* s, float* p, cudaS
 cudaError_t launch_mean_heads(const float* x, int LH, int N, int64_t ld, int zero_below, float* p,
                               cudaStream_t st) {
   ProfScope ps("mean_heads", st);
-  mean_heads_kernel<<<(N + 255) / 256, 256, 0, st>>>(x, LH, N, ld, zero_below, p);
+  mean_heads_kernel<<<(N + 255) / 256, 256, 0, st>>>(x, LH, N, ld, zero_below, 1, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_heads(const float* x, int LH, int N, int64_t ld, int zero_below, float* psum,
+                             cudaStream_t st) {
+  ProfScope ps("sum_heads", st);
+  mean_heads_kernel<<<(N + 255) / 256, 256, 0, st>>>(x, LH, N, ld, zero_below, 0, psum);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sums_to_mean(const float* psum, int N, int heads, float* p, cudaStream_t st) {
+  ProfScope ps("sums_to_mean", st);
+  sums_to_mean_kernel<<<(N + 255) / 256, 256, 0, st>>>(psum, N, heads, p);
+  return cudaGetLastError();
+}
+
+// Per-head scores only (s[lh][i]), no average: the first half of launch_proxy
+// / launch_knorm, for a shard that sums its heads itself.
+cudaError_t launch_proxy_scores(int kind, const void* K, int LH, int N, float* s, cudaStream_t st) {
+  if (kind == 1) {
+    const int64_t rows = static_cast<int64_t>(LH) * N;
+    int64_t blocks = (rows + 16 * 8 - 1) / (16 * 8);
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+    if (blocks > cap) blocks = cap;
+    ProfScope ps("knorm", st);
+    knorm_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(K), rows, s);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(keydiff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  ProfScope ps("keydiff", st);
+  keydiff_kernel<<<dim3(CLUSTER, LH), THREADS, SMEM_BYTES, st>>>(static_cast<const __nv_bfloat16*>(K), N, s);
   return cudaGetLastError();
 }
 

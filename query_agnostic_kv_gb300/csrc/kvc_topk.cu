@@ -676,7 +676,46 @@ cudaError_t launch_cluster(const TopkArgs& A, const EvictParams& P, const EvictC
   return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, A, P, X);
 }
 
+// Largest order key over the non-sink entries of LH rows of N scores.
+__global__ void score_max_kernel(const float* __restrict__ score, int LH, int N, int sinks, uint32_t* key_word) {
+  const int64_t total = static_cast<int64_t>(LH) * N;
+  uint32_t m = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    if (i % N >= sinks) m = max(m, order_key(score[i]));
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0) atomicMax(key_word, m);
+}
+__global__ void key_to_float_kernel(const uint32_t* key_word, float* out) { *out = key_value(*key_word); }
+__global__ void pin_value_kernel(float* __restrict__ score, int LH, int N, int sinks, const float* __restrict__ value) {
+  const float v = *value;
+  const int64_t total = static_cast<int64_t>(LH) * sinks;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    score[(i / sinks) * N + i % sinks] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_score_max(const float* score, int LH, int N, int sinks, uint32_t* key_word, float* max_out,
+                             cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(key_word, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  ProfScope ps("score_max", st);
+  score_max_kernel<<<2 * num_sms(), 256, 0, st>>>(score, LH, N, sinks, key_word);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  key_to_float_kernel<<<1, 1, 0, st>>>(key_word, max_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pin_value(float* score, int LH, int N, int sinks, const float* value, cudaStream_t st) {
+  if (sinks <= 0) return cudaSuccess;
+  ProfScope ps("pin_sinks", st);
+  pin_value_kernel<<<std::max(1, std::min(2 * num_sms(), (LH * sinks + 255) / 256)), 256, 0, st>>>(score, LH, N,
+                                                                                                  sinks, value);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_select(const float* p, int N, int sinks, const ChunkPlan& plan, double rho, int32_t* sel,
                           cudaStream_t st) {

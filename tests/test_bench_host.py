@@ -37,14 +37,18 @@ def test_decode_bytes_count_every_kept_row_once():
     assert bench.decode_bytes(cfg) == cfg.n_seg * cfg.kept * 512 + cfg.n_seg * cfg.G * (256 + 512 + 4)
 
 
-def test_epicache_compaction_bytes_hand_worked():
+def test_epicache_evict_compact_bytes_hand_worked():
     """Blocks of 4, 4, 2 tokens; budgets 5 and 12.  Layer 0 reaches 8 > 5
-    (compacts 5 rows), then 5 + 2 = 7 > 5 (5 rows again); layer 1 stays at or
-    under 12.  Each kept row moves K and V (256 B each, read and written) and
-    its int32 position (read and written): 1032 B per row and KV head."""
+    (reads 8 scores, writes 5 indices, moves 5 rows), then 5 + 2 = 7 > 5
+    (7 scores, 5 indices, 5 rows); layer 1 stays at or under 12.  Each kept
+    row moves K and V (256 B each, read and written) and its int32 position
+    (read and written): 1032 B per row and KV head; scores and indices are
+    4 B each."""
     import types
     cfg = types.SimpleNamespace(L=2, Hkv=3, block=4, sinks=2, n_hist=10)
-    assert bench.epi_compact_bytes(cfg, [5, 12]) == 3 * (5 + 5) * 1032
+    step1 = 8 * 4 + 5 * 4 + 5 * 1032
+    step2 = 7 * 4 + 5 * 4 + 5 * 1032
+    assert bench.epi_evict_compact_bytes(cfg, [5, 12]) == 3 * (step1 + step2)
 
 
 def test_reference_arm_json_line():

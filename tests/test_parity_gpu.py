@@ -425,15 +425,49 @@ EPI_CASES = {
 }
 
 
+def test_tiny_unchained_pipeline(qk):
+    """The tiny workload end to end: the GPU's final kept sets against the
+    oracle's own pipeline (its proxy, selection, scoring and eviction, with no
+    GPU output fed back).  Any difference must lie inside the tie band of the
+    oracle's final scores; the number of differences is printed."""
+    cfg = ks.TINY
+    x = ks.gen_kv2(cfg)
+    L, H, N, S = cfg.L, cfg.Hkv, cfg.N, cfg.sinks
+    shape = (L, H, cfg.Hq, 128, N)
+    K, V, Q = to_dev(x.K), to_dev(x.V), to_dev(x.Q)
+    k = qk.kvc_budget_count(cfg.budget, N, S)
+    ws = torch.empty(qk.kvc_workspace_size(shape, S, cfg.m, cfg.rho), dtype=torch.uint8, device=DEV)
+    kept = torch.empty(L * H * k, dtype=torch.int32, device=DEV)
+    Kc = torch.empty(L * H * k * 128, dtype=torch.bfloat16, device=DEV)
+    Vc = torch.empty_like(Kc)
+    qk.kvc_compress(shape, K, V, Q, S, cfg.m, cfg.rho, 1, [k] * L, kept, Kc, Vc, ws=ws)
+    assert qk.kvc_stream_status() == 0
+    ref = kv2.kv2_compress(kv2.bf16_to_f64(x.K), kv2.bf16_to_f64(x.V), kv2.bf16_to_f64(x.Q), S, cfg.m, cfg.rho,
+                           [k] * L)
+    got = kept.cpu().numpy().reshape(L, H, k)
+    diff = 0
+    for l in range(L):
+        for h in range(H):
+            compare.assert_topk_set(got[l, h], ref["score"][l, h], S, N, k - S, forced=range(S),
+                                    what=f"unchained kept l={l} h={h}")
+            diff += len(set(got[l, h].tolist()) ^ set(ref["kept"][l][h].tolist()))
+    print(f"tiny-4k: {diff} kept positions differ from the oracle's own pipeline")
+
+
 @pytest.mark.parametrize("name", list(EPI_CASES))
 def test_block_prefill_matches_oracle(qk, name):
-    """EpiCache-style streaming with per-layer budgets, small shapes."""
+    """EpiCache-style streaming with per-layer budgets, small shapes, checked
+    step by step: every over-budget step of every layer is compared with one
+    oracle step started from the GPU's state before it -- the step's scores
+    element-wise (1e-3 relative, read from the workspace), the kept set up to
+    oracle near-ties within 1e-4 of the threshold, the kept K and V rows bit
+    for bit; an under-budget step must append the block unchanged."""
     cfg = ks.EpiConfig(name, d=128, n_hist=1500, block=256, episodes=1, prompt_len=24, alpha=3.0, sinks=4,
                        **EPI_CASES[name])
     sens = ks.gen_sensitivity(cfg)
     budgets = qk.kvc_layer_budgets(sens.tolist(), cfg.alpha, cfg.mean_budget, cfg.sinks)
     assert budgets == kv2.layer_budgets(sens.astype(np.float64), cfg.alpha, cfg.mean_budget, cfg.sinks).tolist()
-    L, H, Hq, B, P = cfg.L, cfg.Hkv, cfg.Hq, cfg.block, cfg.prompt_len
+    L, H, Hq, B, P, S = cfg.L, cfg.Hkv, cfg.Hq, cfg.block, cfg.prompt_len, cfg.sinks
     hist = [ks.gen_epi_history_layer(cfg, l) for l in range(L)]
     Kh = np.stack([h[0] for h in hist]); Vh = np.stack([h[1] for h in hist])
     prm = [ks.gen_epi_prompt_layer(cfg, 0, l) for l in range(L)]
@@ -441,37 +475,54 @@ def test_block_prefill_matches_oracle(qk, name):
     cap = max(budgets) + B
     slabs = [torch.zeros(L * H * cap * 128, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
     pos = [torch.zeros(L * H * cap, dtype=torch.int32, device=DEV) for _ in range(2)]
-    st = qk.kvc_block_state_init(L, H, Hq, cap, cfg.sinks, budgets, slabs[0], slabs[1], pos[0], slabs[2], slabs[3],
-                                 pos[1])
+    st = qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0], slabs[2], slabs[3], pos[1])
     ws = torch.empty(qk.kvc_block_workspace_size(st, B, P), dtype=torch.uint8, device=DEV)
     Qp_d, Kp_d = to_dev(Qp), to_dev(Kp)
+    Kf = [kv2.bf16_to_f64(Kh[l]) for l in range(L)]
+    Qf = [kv2.bf16_to_f64(Qp[l]) for l in range(L)]
+    Kpf = [kv2.bf16_to_f64(Kp[l]) for l in range(L)]
+    scored = 0
     for t0 in range(0, cfg.n_hist, B):
         t1 = min(t0 + B, cfg.n_hist)
+        prev = [pos[st.cur[l]].view(L, H, cap)[l, :, :st.len[l]].cpu().numpy().astype(np.int64) for l in range(L)]
         kb = to_dev(np.ascontiguousarray(Kh[:, :, t0:t1]))
         vb = to_dev(np.ascontiguousarray(Vh[:, :, t0:t1]))
         qk.kvc_block_prefill_step(st, kb, vb, t1 - t0, Qp_d, Kp_d, P, ws=ws)
         assert qk.kvc_stream_status() == 0
-    Kst_all = [bits_of(slabs[0]).reshape(L, H, cap, 128), bits_of(slabs[2]).reshape(L, H, cap, 128)]
-    pst_all = [pos[0].cpu().numpy().reshape(L, H, cap), pos[1].cpu().numpy().reshape(L, H, cap)]
-    same = total = 0
+        step_scores = ws[:L * H * cap * 4].view(torch.float32).cpu().numpy().reshape(L, H, cap).astype(np.float64)
+        for l in range(L):
+            n = st.len[l]
+            c = st.cur[l]
+            got_pos = pos[c].view(L, H, cap)[l, :, :n].cpu().numpy().astype(np.int64)
+            got_K = bits_of(slabs[2 * c]).reshape(L, H, cap, 128)[l, :, :n]
+            got_V = bits_of(slabs[2 * c + 1]).reshape(L, H, cap, 128)[l, :, :n]
+            cat_pos = np.concatenate([prev[l], np.broadcast_to(np.arange(t0, t1), (H, t1 - t0))], axis=1)
+            n_cat = cat_pos.shape[1]
+            for h in range(H):
+                np.testing.assert_array_equal(got_K[h], Kh[l, h][got_pos[h]])
+                np.testing.assert_array_equal(got_V[h], Vh[l, h][got_pos[h]])
+            if n_cat <= budgets[l]:
+                assert np.array_equal(got_pos, cat_pos), (t0, l)
+                continue
+            # one oracle step from the GPU's previous state
+            Kcat = np.stack([Kf[l][h][cat_pos[h]] for h in range(H)])
+            sc = kv2.block_step_scores(Kcat, Qf[l], Kpf[l], S)
+            for h in range(H):
+                compare.assert_scores(step_scores[l, h, S:n_cat], sc[h, S:], floor=0.0,
+                                      what=f"block {t0} layer {l} head {h} scores")
+                idx = np.searchsorted(cat_pos[h], got_pos[h])
+                assert np.array_equal(cat_pos[h][idx], got_pos[h])
+                compare.assert_topk_set(idx, sc[h], S, n_cat, budgets[l] - S, forced=range(S),
+                                        what=f"block {t0} layer {l} head {h} kept")
+            scored += 1
+    assert scored > 0
+    # for information: the final caches against the unchained oracle
+    diff = 0
     for l in range(L):
-        ref = kv2.block_prefill_layer(kv2.bf16_to_f64(Kh[l]), kv2.bf16_to_f64(Vh[l]), kv2.bf16_to_f64(Qp[l]),
-                                      kv2.bf16_to_f64(Kp[l]), B, budgets[l], cfg.sinks)
-        n = st.len[l]
-        assert n == ref[0].shape[1]
-        c = st.cur[l]
-        Kst, pst = Kst_all[c], pst_all[c]
-        for h in range(H):
-            got = pst[l, h, :n]
-            assert np.all(np.diff(got) > 0) and set(range(cfg.sinks)) <= set(got.tolist())
-            np.testing.assert_array_equal(Kst[l, h, :n], Kh[l, h][got])
-            # near-ties aside the kept global positions agree with the oracle:
-            # at most one swapped pair per head, 99.5% over all heads
-            g, r = set(got.tolist()), set(ref[2][h].tolist())
-            assert len(g ^ r) <= 2, (l, h, sorted(g - r), sorted(r - g))
-            same += len(g & r)
-            total += n
-    assert same / total > 0.995, same / total
+        ref = kv2.block_prefill_layer(Kf[l], kv2.bf16_to_f64(Vh[l]), Qf[l], Kpf[l], B, budgets[l], S)
+        got = pos[st.cur[l]].view(L, H, cap)[l, :, :st.len[l]].cpu().numpy()
+        diff += sum(len(set(got[h].tolist()) ^ set(ref[2][h].tolist())) for h in range(H))
+    print(f"{name}: {scored} scored layer steps; {diff} positions differ from the unchained oracle")
 
 
 @pytest.mark.slow
