@@ -7,6 +7,8 @@
 // row, so reads and writes stay fully coalesced.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "kvc_internal.h"
 #include "kvc_ptx.cuh"
 
@@ -16,11 +18,20 @@ namespace {
 constexpr int THREADS = 256;
 constexpr int ROWS_PER_BLOCK = 64;  // 16 half-warps x 4 rows
 
-__global__ void __launch_bounds__(THREADS) compact_kernel(const uint4* __restrict__ K, const uint4* __restrict__ V,
-                                                          const int32_t* __restrict__ idx,
-                                                          const int32_t* __restrict__ pos_src,
-                                                          int32_t* __restrict__ pos_dst, uint4* __restrict__ Kc,
-                                                          uint4* __restrict__ Vc,
+// Source and destination of layer l: the single buffers of a plain
+// compaction, or (per-layer slabs) slab[l] -> its other slab.
+struct CompactBufs {
+  const uint4* K[2];
+  const uint4* V[2];
+  const int32_t* pos[2];
+  uint4* Kd[2];
+  uint4* Vd[2];
+  int32_t* posd[2];
+  int32_t slab[kMaxLayers];
+};
+
+__global__ void __launch_bounds__(THREADS) compact_kernel(const int32_t* __restrict__ idx,
+                                                          const __grid_constant__ CompactBufs X,
                                                           const __grid_constant__ CompactParams P, int* status) {
   // One block per (layer, KV head, 64-row tile) of the active layers only:
   // layer l owns blocks [unit_off[l], unit_off[l+1]), head-major.  Budgets
@@ -33,6 +44,13 @@ __global__ void __launch_bounds__(THREADS) compact_kernel(const uint4* __restric
     if (P.unit_off[mid] <= u) l = mid; else hi = mid;
   }
   const int k = P.k[l];
+  const int sl = X.slab[l];
+  const uint4* K = X.K[sl];
+  const uint4* V = X.V[sl];
+  const int32_t* pos_src = X.pos[sl];
+  uint4* Kc = X.Kd[sl];
+  uint4* Vc = X.Vd[sl];
+  int32_t* pos_dst = X.posd[sl];
   const int tiles = (k + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK;
   const int r = u - P.unit_off[l];
   const int h = r / tiles;
@@ -98,8 +116,8 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const uint4* __restrict
 
 }  // namespace
 
-cudaError_t launch_compact(const void* K, const void* V, const int32_t* idx, const int32_t* pos_src,
-                           int32_t* pos_dst, void* Kc, void* Vc, const CompactParams& cp, cudaStream_t st) {
+namespace {
+cudaError_t launch_compact_bufs(const int32_t* idx, const CompactBufs& X, const CompactParams& cp, cudaStream_t st) {
   CompactParams p = cp;
   int64_t units = 0;
   for (int l = 0; l < p.L; ++l) {
@@ -113,10 +131,37 @@ cudaError_t launch_compact(const void* K, const void* V, const int32_t* idx, con
   if (units == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(units));
   ProfScope ps("compact", st);
-  compact_kernel<<<grid, THREADS, 0, st>>>(static_cast<const uint4*>(K), static_cast<const uint4*>(V), idx, pos_src,
-                                           pos_dst, static_cast<uint4*>(Kc), static_cast<uint4*>(Vc), p,
-                                           status_word());
+  compact_kernel<<<grid, THREADS, 0, st>>>(idx, X, p, status_word());
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_compact(const void* K, const void* V, const int32_t* idx, const int32_t* pos_src,
+                           int32_t* pos_dst, void* Kc, void* Vc, const CompactParams& cp, cudaStream_t st) {
+  CompactBufs X;
+  memset(&X, 0, sizeof(X));
+  X.K[0] = static_cast<const uint4*>(K);
+  X.V[0] = static_cast<const uint4*>(V);
+  X.pos[0] = pos_src;
+  X.Kd[0] = static_cast<uint4*>(Kc);
+  X.Vd[0] = static_cast<uint4*>(Vc);
+  X.posd[0] = pos_dst;
+  return launch_compact_bufs(idx, X, cp, st);
+}
+
+cudaError_t launch_compact_slabs(const int32_t* idx, const EvictCopy& copy, const CompactParams& cp, cudaStream_t st) {
+  CompactBufs X;
+  memset(&X, 0, sizeof(X));
+  for (int i = 0; i < 2; ++i) {
+    X.K[i] = static_cast<const uint4*>(copy.K[i]);
+    X.V[i] = static_cast<const uint4*>(copy.V[i]);
+    X.pos[i] = copy.pos[i];
+    X.Kd[i] = static_cast<uint4*>(copy.Kd[i]);
+    X.Vd[i] = static_cast<uint4*>(copy.Vd[i]);
+    X.posd[i] = copy.posd[i];
+  }
+  for (int l = 0; l < cp.L; ++l) X.slab[l] = copy.slab[l];
+  return launch_compact_bufs(idx, X, cp, st);
 }
 
 cudaError_t launch_append(const void* Kblk, const void* Vblk, void* K0, void* V0, int32_t* pos0, void* K1, void* V1,

@@ -154,6 +154,11 @@ struct EvictCopy {
 // order key, an arrival counter).  copy: null, or the fused compaction.
 cudaError_t launch_evict(float* score, const EvictParams& ep, int32_t* kept, uint32_t* gmax_word, bool pin,
                          const EvictCopy* copy, cudaStream_t st);
+// The eviction kernel copies the kept rows itself (one launch) when a row
+// keeps at most kFusedCopyRows rows; longer kept lists move in one tiled
+// compaction launch after it (a row's copy would otherwise fall to a
+// single CTA).
+constexpr int kFusedCopyRows = 4096;
 
 // Compaction: dst row (l, h, t) = src row (l, h, idx[l][h][t]).
 struct CompactParams {
@@ -169,6 +174,10 @@ struct CompactParams {
 };
 cudaError_t launch_compact(const void* K, const void* V, const int32_t* idx, const int32_t* pos_src,
                            int32_t* pos_dst, void* Kc, void* Vc, const CompactParams& cp, cudaStream_t st);
+
+// The same with each layer's rows going from copy.K[slab[l]] (and V, pos)
+// to copy.Kd[slab[l]] (EpiCache slabs: one launch for both directions).
+cudaError_t launch_compact_slabs(const int32_t* idx, const EvictCopy& copy, const CompactParams& cp, cudaStream_t st);
 
 // Block append: state rows [len_l, len_l + B) of each (l, h) <- block rows.
 struct AppendParams {

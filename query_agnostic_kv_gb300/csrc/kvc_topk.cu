@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(CT, 2)
   // ---- 4. ordered emit; for the fused copy the CTA's positions are also
   // kept in shared memory (in the histogram area, free by now) when they fit
   constexpr int kSposCap = CW * 256;
+  static_assert(kSposCap >= kFusedCopyRows, "a fused copy keeps its positions in shared memory");
   int32_t* spos = (A.copy && sm.sel_cta <= static_cast<uint32_t>(kSposCap))
                       ? reinterpret_cast<int32_t*>(&sm.whist[0][0]) : nullptr;
   {
@@ -641,6 +642,25 @@ bool plan_parts(int64_t len, int* parts, int* part_keys) {
   return true;
 }
 
+// Tiled compaction of the kept rows of every active layer, one launch.
+cudaError_t compact_after(const EvictParams& ep, const int32_t* kept, const EvictCopy& copy, cudaStream_t st) {
+  CompactParams cp;
+  memset(&cp, 0, sizeof(cp));
+  cp.L = ep.L;
+  cp.Hkv = ep.Hkv;
+  cp.src_ld = copy.src_ld;
+  cp.dst_ld = copy.dst_ld;
+  for (int l = 0; l < ep.L; ++l) {
+    if (!ep.active[l]) continue;
+    cp.n_src[l] = ep.n[l];
+    cp.k[l] = ep.k[l];
+    cp.idx_off[l] = ep.out_off[l];
+    cp.dst_off[l] = ep.out_off[l];
+    cp.active[l] = 1;
+  }
+  return launch_compact_slabs(kept, copy, cp, st);
+}
+
 cudaError_t launch_cluster(const TopkArgs& A, const EvictParams& P, const EvictCopy& X, int parts, int part_keys,
                            dim3 grid, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(part_keys) * sizeof(uint32_t);
@@ -766,6 +786,9 @@ cudaError_t launch_evict(float* score, const EvictParams& ep, int32_t* kept, uin
     longest = std::max<int64_t>(longest, static_cast<int64_t>(ep.n[l]) - ep.sinks);
   }
   if (n_act == 0) return cudaSuccess;
+  int kmax = 0;
+  for (int a = 0; a < n_act; ++a) kmax = std::max(kmax, ep.k[A.act[a]]);
+  const bool fuse = copy != nullptr && kmax <= kFusedCopyRows;
   int parts = 1, part_keys = 4;
   if (ep.Hkv <= 65535 && plan_parts(longest, &parts, &part_keys)) {
     A.mode = 1;
@@ -774,16 +797,21 @@ cudaError_t launch_evict(float* score, const EvictParams& ep, int32_t* kept, uin
     A.kept = kept;
     A.gmax = want_pin ? gmax_word : nullptr;
     A.total_ctas = parts * ep.Hkv * n_act;
-    A.copy = copy != nullptr;
+    A.copy = fuse;
     EvictCopy X;
     if (copy)
       X = *copy;
     else
       memset(&X, 0, sizeof(X));
-    ProfScope ps(copy ? "evict_compact" : "evict_topk", st);
-    cudaError_t e = launch_cluster(A, ep, X, parts, part_keys, dim3(parts, ep.Hkv, n_act), st);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    {
+      ProfScope ps(fuse ? "evict_compact" : "evict_topk", st);
+      cudaError_t e = launch_cluster(A, ep, X, parts, part_keys, dim3(parts, ep.Hkv, n_act), st);
+      if (e != cudaSuccess) return e;
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    if (!copy || fuse) return cudaSuccess;
+    return compact_after(ep, kept, *copy, st);
   }
   // rows too long for the shared-memory parts
   dim3 grid(ep.Hkv, ep.L);
@@ -800,29 +828,7 @@ cudaError_t launch_evict(float* score, const EvictParams& ep, int32_t* kept, uin
     if (e != cudaSuccess) return e;
   }
   if (!copy) return cudaSuccess;
-  for (int from = 0; from < 2; ++from) {
-    CompactParams cp;
-    memset(&cp, 0, sizeof(cp));
-    cp.L = ep.L;
-    cp.Hkv = ep.Hkv;
-    cp.src_ld = copy->src_ld;
-    cp.dst_ld = copy->dst_ld;
-    bool any = false;
-    for (int l = 0; l < ep.L; ++l) {
-      if (!ep.active[l] || copy->slab[l] != from) continue;
-      cp.n_src[l] = ep.n[l];
-      cp.k[l] = ep.k[l];
-      cp.idx_off[l] = ep.out_off[l];
-      cp.dst_off[l] = ep.out_off[l];
-      cp.active[l] = 1;
-      any = true;
-    }
-    if (!any) continue;
-    e = launch_compact(copy->K[from], copy->V[from], kept, copy->pos[from], copy->posd[from], copy->Kd[from],
-                       copy->Vd[from], cp, st);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return compact_after(ep, kept, *copy, st);
 }
 
 }  // namespace kvc

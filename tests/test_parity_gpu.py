@@ -419,6 +419,9 @@ def test_bounds_status_path(qk):
 
 EPI_CASES = {
     "epi-small": dict(L=3, Hkv=2, Hq=6, mean_budget=300),
+    # budgets above 4096: the kept rows move in a separate tiled compaction
+    # launch (one launch for both slab directions)
+    "epi-long-kept": dict(L=3, Hkv=2, Hq=6, mean_budget=5000, n_hist=14000, block=2048),
     # 20 x 8 over-budget heads at the last blocks: 160 row-LSE units of
     # different lengths on 152 SMs, so the second, reversed wave is taken
     "epi-20x8": dict(L=20, Hkv=8, Hq=24, mean_budget=600),
@@ -462,8 +465,9 @@ def test_block_prefill_matches_oracle(qk, name):
     element-wise (1e-3 relative, read from the workspace), the kept set up to
     oracle near-ties within 1e-4 of the threshold, the kept K and V rows bit
     for bit; an under-budget step must append the block unchanged."""
-    cfg = ks.EpiConfig(name, d=128, n_hist=1500, block=256, episodes=1, prompt_len=24, alpha=3.0, sinks=4,
-                       **EPI_CASES[name])
+    case = dict(n_hist=1500, block=256)
+    case.update(EPI_CASES[name])
+    cfg = ks.EpiConfig(name, d=128, episodes=1, prompt_len=24, alpha=3.0, sinks=4, **case)
     sens = ks.gen_sensitivity(cfg)
     budgets = qk.kvc_layer_budgets(sens.tolist(), cfg.alpha, cfg.mean_budget, cfg.sinks)
     assert budgets == kv2.layer_budgets(sens.astype(np.float64), cfg.alpha, cfg.mean_budget, cfg.sinks).tolist()
