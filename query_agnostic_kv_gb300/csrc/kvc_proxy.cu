@@ -262,19 +262,29 @@ __global__ void __launch_bounds__(256) knorm_kernel(const uint4* __restrict__ K,
   }
 }
 
-// p[i] = (1/LH) sum_h x[h][i] (fixed order), 0 below `zero_below`; with
-// `divide` 0 the plain sum (a shard's partial sum for the layer-sharded path).
-__global__ void mean_heads_kernel(const float* __restrict__ x, int LH, int N, int64_t ld, int zero_below, int divide,
-                                  float* __restrict__ p) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N) return;
-  if (i < zero_below) {
-    p[i] = 0.f;
-    return;
-  }
+// p[i] = (1/LH) sum_h x[h][i], 0 below `zero_below`; with `divide` 0 the
+// plain sum (a shard's partial sum for the layer-sharded path).  A block
+// covers 32 positions with 8 warps: warp w adds heads w, w + 8, ... of its
+// lane's position (coalesced 128-byte rows), and the eight partial sums are
+// then added in warp order, so the result does not depend on scheduling.
+constexpr int MH_POS = 32, MH_SPLIT = 8;
+__global__ void __launch_bounds__(MH_POS* MH_SPLIT)
+    mean_heads_kernel(const float* __restrict__ x, int LH, int N, int64_t ld, int zero_below, int divide,
+                      float* __restrict__ p) {
+  __shared__ float part[MH_SPLIT][MH_POS];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int i = blockIdx.x * MH_POS + lane;
   float t = 0.f;
-  for (int h = 0; h < LH; ++h) t += x[static_cast<int64_t>(h) * ld + i];
-  p[i] = divide ? t / static_cast<float>(LH) : t;
+  if (i < N && i >= zero_below)
+    for (int h = w; h < LH; h += MH_SPLIT) t += x[static_cast<int64_t>(h) * ld + i];
+  part[w][lane] = t;
+  __syncthreads();
+  if (w == 0 && i < N) {
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < MH_SPLIT; ++q) s += part[q][lane];
+    p[i] = i < zero_below ? 0.f : (divide ? s / static_cast<float>(LH) : s);
+  }
 }
 
 // p[i] = psum[i] / heads (the division of the unsharded mean, applied to the
@@ -293,9 +303,20 @@ size_t proxy_scratch_bytes(int LH, int N) {
   return 0;
 }
 
+// The KeyDiff kernel's shared-memory attribute, set once per device.
+cudaError_t keydiff_attr() {
+  static int done[64];
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  if (done[d]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(keydiff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess) done[d] = 1;
+  return e;
+}
+
 cudaError_t launch_proxy(const void* K, int LH, int N, float* s, float* p, void* scratch, cudaStream_t st) {
   (void)scratch;
-  cudaError_t e = cudaFuncSetAttribute(keydiff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = keydiff_attr();
   if (e != cudaSuccess) return e;
   dim3 grid(CLUSTER, LH);
   {
@@ -324,14 +345,14 @@ cudaError_t launch_knorm(const void* K, int LH, int N, float* s, float* p, cudaS
 cudaError_t launch_mean_heads(const float* x, int LH, int N, int64_t ld, int zero_below, float* p,
                               cudaStream_t st) {
   ProfScope ps("mean_heads", st);
-  mean_heads_kernel<<<(N + 255) / 256, 256, 0, st>>>(x, LH, N, ld, zero_below, 1, p);
+  mean_heads_kernel<<<(N + MH_POS - 1) / MH_POS, MH_POS * MH_SPLIT, 0, st>>>(x, LH, N, ld, zero_below, 1, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_sum_heads(const float* x, int LH, int N, int64_t ld, int zero_below, float* psum,
                              cudaStream_t st) {
   ProfScope ps("sum_heads", st);
-  mean_heads_kernel<<<(N + 255) / 256, 256, 0, st>>>(x, LH, N, ld, zero_below, 0, psum);
+  mean_heads_kernel<<<(N + MH_POS - 1) / MH_POS, MH_POS * MH_SPLIT, 0, st>>>(x, LH, N, ld, zero_below, 0, psum);
   return cudaGetLastError();
 }
 
@@ -353,7 +374,7 @@ cudaError_t launch_proxy_scores(int kind, const void* K, int LH, int N, float* s
     knorm_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(K), rows, s);
     return cudaGetLastError();
   }
-  cudaError_t e = cudaFuncSetAttribute(keydiff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = keydiff_attr();
   if (e != cudaSuccess) return e;
   ProfScope ps("keydiff", st);
   keydiff_kernel<<<dim3(CLUSTER, LH), THREADS, SMEM_BYTES, st>>>(static_cast<const __nv_bfloat16*>(K), N, s);

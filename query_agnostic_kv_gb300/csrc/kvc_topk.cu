@@ -677,22 +677,24 @@ cudaError_t launch_cluster(const TopkArgs& A, const EvictParams& P, const EvictC
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // two CTAs of a 64 KB part share an SM only with the largest shared-memory carveout
-  if (parts > 1) {
-    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  // Two CTAs of a 64 KB part share an SM only with the largest shared-memory
+  // carveout.  Attributes are set once per device (for the largest part size),
+  // not on every launch.
+  static int attr_done[64][2];
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  const int multi = parts > 1 ? 1 : 0;
+  if (!attr_done[d][multi]) {
+    const void* fn = multi ? reinterpret_cast<const void*>(topk_cluster_kernel<true>)
+                           : reinterpret_cast<const void*>(topk_cluster_kernel<false>);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPartKeysMax * sizeof(uint32_t)));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(topk_cluster_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, A, P, X);
+    attr_done[d][multi] = 1;
   }
-  cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(topk_cluster_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
+  if (multi) return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, A, P, X);
   return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, A, P, X);
 }
 
