@@ -58,6 +58,9 @@ def parse():
                          "epicache: EpiCache block prefill of every episode; rho: the compression step at "
                          "several reconstruction ratios")
     ap.add_argument("--decode-config", default=ks.DECODE_128K.name, choices=list(ks.DECODE_CONFIGS))
+    ap.add_argument("--epi-layout", choices=["two-slab", "one-slab"], default="one-slab",
+                    help="EpiCache block state: kept rows compacted into the other slab every step, or kept in "
+                         "place with the kept block rows moved into evicted rows")
     return ap.parse_args()
 
 
@@ -1206,6 +1209,33 @@ def epi_evict_compact_bytes(cfg, budgets):
     return total
 
 
+def epi_in_place_bytes(qk, cfg, budgets, new_state, blocks, prompt, ws, stream, pos0, cap):
+    """Algorithmic bytes of the one-slab eviction launches over one episode,
+    replayed untimed: an over-budget layer reads the n scores of each KV head
+    and moves each kept block row that was appended at or above its budget
+    into an evicted row (K and V rows read and written, positions read and
+    written).  Such a row has position >= t0 + M_l - len_l."""
+    import torch
+    B, S, L, H = cfg.block, cfg.sinks, cfg.L, cfg.Hkv
+    st = new_state()
+    dq, dk = prompt
+    total = 0
+    t0 = 0
+    for kb, vb, n in blocks:
+        old = [st.len[l] for l in range(L)]
+        qk.kvc_block_prefill_step(st, kb, vb, n, dq, dk, cfg.prompt_len, ws=ws, stream=stream)
+        P = pos0.view(L, H, cap)
+        for l in range(L):
+            if old[l] + n > budgets[l] and old[l] + n > S:
+                first = t0 + max(budgets[l] - old[l], 0)
+                p = P[l, :, :budgets[l]]
+                moved = int(((p >= first) & (p < t0 + n)).sum())
+                total += H * (old[l] + n) * 4 + moved * (2 * 2 * 128 * 2 + 2 * 4)
+        t0 += n
+    torch.cuda.synchronize()
+    return total
+
+
 # DRAM bytes (read + write) per eviction + compaction launch of the EpiCache
 # block step, from ncu; None until captured for the fused kernel.
 EPI_EVICT_TRAFFIC_PER_LAUNCH = None
@@ -1256,16 +1286,23 @@ def run_epicache(args, rank, world, local_rank):
     cap = max(budgets) + B
     torch.cuda.synchronize()
     mem0 = torch.cuda.memory_allocated(dev)
-    slabs = [torch.zeros(L * H * cap * 128, dtype=torch.bfloat16, device=dev) for _ in range(4)]
-    pos = [torch.zeros(L * H * cap, dtype=torch.int32, device=dev) for _ in range(2)]
+    n_slab = 2 if args.epi_layout == "two-slab" else 1
+    slabs = [torch.zeros(L * H * cap * 128, dtype=torch.bfloat16, device=dev) for _ in range(2 * n_slab)]
+    pos = [torch.zeros(L * H * cap, dtype=torch.int32, device=dev) for _ in range(n_slab)]
+
+    def new_state():
+        if n_slab == 2:
+            return qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0], slabs[2],
+                                           slabs[3], pos[1])
+        return qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0])
+
     stream = torch.cuda.current_stream()
     blocks = [(Kblk[b] if b < nb - 1 or cfg.n_hist % B == 0 else Kblk[b, :, :, :cfg.n_hist - b * B].contiguous(),
                Vblk[b] if b < nb - 1 or cfg.n_hist % B == 0 else Vblk[b, :, :, :cfg.n_hist - b * B].contiguous(),
                min(B, cfg.n_hist - b * B)) for b in range(nb)]
 
     def episode(e, ws=None):
-        st = qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0], slabs[2], slabs[3],
-                                     pos[1])
+        st = new_state()
         if ws is None:
             ws = torch.empty(qk.kvc_block_workspace_size(st, B, P), dtype=torch.uint8, device=dev)
         dq, dk = prompts[e]
@@ -1277,10 +1314,11 @@ def run_epicache(args, rank, world, local_rank):
     ws = episode(0)
     torch.cuda.synchronize()
     memory = {
+        "layout": args.epi_layout,
         "block_state_and_workspace_bytes": torch.cuda.memory_allocated(dev) - mem0,
         "workspace_bytes": ws.numel(),
         "full_kv_cache_of_history_bytes": 2 * L * H * cfg.n_hist * 128 * 2,
-        "how": "device bytes allocated for the two K/V slabs, the position arrays and the step workspace (torch "
+        "how": "device bytes allocated for the K/V slabs, the position arrays and the step workspace (torch "
                "allocator, measured), against the K and V of the whole history (computed from its shape); the "
                "model weights and the history blocks themselves are not counted",
     }
@@ -1311,17 +1349,26 @@ def run_epicache(args, rank, world, local_rank):
     total = sum(v[1] for v in prof.values())
     kernels = {n: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / total} for n, v in prof.items()}
 
-    # roofline of eviction + compaction (one fused launch when the kept lists
-    # are short, else the eviction launch and one tiled compaction launch),
-    # bound by HBM
+    # roofline of eviction + compaction, bound by HBM.  Two slabs: one fused
+    # launch when the kept lists are short, else the eviction launch and one
+    # tiled compaction launch.  One slab: one launch moving the kept block
+    # rows into evicted rows; how many rows moved is counted in an untimed
+    # replay of the same episodes.
     peaks, peak_src = load_peaks()
     hbm = peaks.get("hbm_gbs")
-    cbytes = epi_evict_compact_bytes(cfg, budgets) * cfg.episodes
-    parts = [n for n in ("evict_compact", "evict_topk", "compact") if n in prof]
+    if n_slab == 2:
+        cbytes = epi_evict_compact_bytes(cfg, budgets) * cfg.episodes
+        parts = [n for n in ("evict_compact", "evict_topk", "compact") if n in prof]
+        what = "top-M_l per KV head, kept rows into the other slab"
+    else:
+        cbytes = sum(epi_in_place_bytes(qk, cfg, budgets, new_state, blocks, prompts[e], ws, stream, pos[0], cap)
+                     for e in range(cfg.episodes))
+        parts = ["evict_in_place"]
+        what = "top-M_l per KV head, kept block rows into evicted rows"
     ctime = sum(prof[n][1] for n in parts) / 1e3
-    steps_scored = prof["evict_compact"][0] if "evict_compact" in prof else prof["evict_topk"][0]
+    steps_scored = sum(prof[n][0] for n in ("evict_compact", "evict_topk", "evict_in_place") if n in prof)
     ach = cbytes / ctime / 1e9
-    roof = {"kernel": " + ".join(parts) + " (top-M_l per KV head, kept rows into the other slab)", "bound": "hbm",
+    roof = {"kernel": " + ".join(parts) + f" ({what})", "bound": "hbm",
             "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
             "traffic": EPI_EVICT_TRAFFIC_PER_LAUNCH,
             "traffic_source": "ncu dram bytes per step (null: not captured for these kernels)",
@@ -1344,8 +1391,7 @@ def run_epicache(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
         def episode_host(e, start=None):
-            st = qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0], slabs[2],
-                                         slabs[3], pos[1])
+            st = new_state()
             dq, dk = prompts[e]
             for i, (hk, hv, n) in enumerate(hblocks):
                 j = i % 2
@@ -1388,8 +1434,8 @@ def run_epicache(args, rank, world, local_rank):
         "metric": EPI_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": cfg.episodes,
         "warmup": n_warm, "ms_per_step": ms / cfg.episodes, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name, "L": L, "Hkv": H, "Hq": Hq, "n_hist": cfg.n_hist, "block": B,
-                   "episodes": cfg.episodes, "prompt_queries": P, "mean_budget": cfg.mean_budget, "alpha": cfg.alpha,
+        "config": {"workload": cfg.name, "layout": args.epi_layout, "L": L, "Hkv": H, "Hq": Hq,
+                   "n_hist": cfg.n_hist, "block": B, "episodes": cfg.episodes, "prompt_queries": P, "mean_budget": cfg.mean_budget, "alpha": cfg.alpha,
                    "step": "one episode (all history blocks)", "l2": "history 10 GB on the device"},
         "roofline": roof, "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()), "clocks": clocks,
         "memory": memory, "e2e": e2e, "cpu_baseline": cpu}), flush=True)

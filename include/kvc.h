@@ -338,9 +338,18 @@ KVC_API kvc_status kvc_layer_budgets(const float* sens, int32_t L, double alpha,
 #define KVC_MAX_LAYERS 128
 
 /* State of one episode's block prefill.  Device buffers are caller-owned;
- * the host fields are maintained by the library.  Every layer lives in one
- * of two slabs (cur[l]); compaction moves the kept rows of a layer into the
- * other slab, so a layer's rows are always at slab cur[l], rows [0, len[l]). */
+ * the host fields are maintained by the library.  A layer's rows are always
+ * at slab cur[l], rows [0, len[l]), in one of two layouts chosen at init:
+ *   two slabs  every step moves the kept rows of each over-budget layer into
+ *              its other slab in ascending position order (the EpiCache
+ *              page's cache after every step, row order = position order);
+ *   one slab   (K[1], V[1], pos[1] NULL, cur[l] always 0) kept rows stay
+ *              where they are and each kept row of the new block moves into
+ *              the row of an evicted one, so a step moves at most one block
+ *              of rows and the state needs half the memory; rows are in no
+ *              particular order (pos[0] holds each row's position) until
+ *              kvc_episode_pack writes them in ascending position order.
+ * Both keep the same rows at every step. */
 typedef struct {
   int32_t L, Hkv, Hq, d;
   int32_t capacity;               /* rows per (layer, KV head) in each slab: >= max budget + block */
@@ -355,8 +364,10 @@ typedef struct {
 } kvc_block_state;
 
 /* Initialises `st` for an empty cache (no device work).  Each slab must hold
- * L*Hkv*capacity rows.  Invalid: L > KVC_MAX_LAYERS, d != 128, a budget
- * below `sinks`, capacity below the largest budget. */
+ * L*Hkv*capacity rows.  K1, V1 and pos1 all NULL select the one-slab layout
+ * (capacity at most 393216 rows then).  Invalid: L > KVC_MAX_LAYERS,
+ * d != 128, a budget below `sinks`, capacity below the largest budget, some
+ * but not all of K1, V1, pos1 NULL. */
 KVC_API kvc_status kvc_block_state_init(kvc_block_state* st, int32_t L, int32_t Hkv, int32_t Hq, int32_t d, int32_t capacity,
                                 int32_t sinks, const int32_t* budgets, void* K0, void* V0, int32_t* pos0, void* K1,
                                 void* V1, int32_t* pos1);
@@ -375,8 +386,10 @@ KVC_API size_t kvc_block_workspace_size(const kvc_block_state* st, int32_t max_b
  * more than its budget M_l scores its non-sink rows against the episode's
  * patched prompt (the KV² max rule with the prompt's P queries appended
  * causally, prompt keys as the appended keys), pins the sinks, keeps the M_l
- * best rows per KV head (lower global position wins a tie) in position
- * order and compacts.  Peak cache size stays at M_l + block.
+ * best rows per KV head (lower global position wins a tie) and compacts
+ * them: into the other slab in position order (two slabs), or by moving the
+ * kept block rows into evicted rows (one slab).  Peak cache size stays at
+ * M_l + block.
  *   Kblk, Vblk  device bf16 [L][Hkv][blk_len][d]
  *   Qprompt     device bf16 [L][Hq][P][d]
  *   Kprompt     device bf16 [L][Hkv][P][d]
@@ -445,7 +458,8 @@ KVC_API int64_t kvc_episode_rows(const kvc_block_state* st);
 /* Packs the kept rows of a block-prefill state into one contiguous image in
  * the compacted layout (segment (l, h) holds len[l] rows; kvc_compact_segments
  * with k_l = len[l] addresses it), so one copy moves the whole episode and
- * kvc_decode_attention reads it in place.
+ * kvc_decode_attention reads it in place.  Every segment's rows are in
+ * ascending position order, in either state layout.
  *   Kp, Vp    device bf16 [kvc_episode_rows][128] (output)
  *   pos_opt   device int32 [kvc_episode_rows] global positions, or NULL */
 KVC_API kvc_status kvc_episode_pack(const kvc_block_state* st, void* Kp, void* Vp, int32_t* pos_opt,

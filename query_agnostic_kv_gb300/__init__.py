@@ -565,8 +565,9 @@ def kvc_q4_decode(codes, params, X, stream=None) -> None:
 
 
 # ---------------------------------------------------------------- EpiCache block prefill
-def kvc_block_state_init(L, Hkv, Hq, capacity, sinks, budgets, K0, V0, pos0, K1, V1, pos1,
+def kvc_block_state_init(L, Hkv, Hq, capacity, sinks, budgets, K0, V0, pos0, K1=None, V1=None, pos1=None,
                          d: int = 128) -> kvc_block_state:
+    """K1, V1, pos1 None: the one-slab layout (kept rows stay in place)."""
     st = kvc_block_state()
     _check("kvc_block_state_init", lib().kvc_block_state_init(
         ctypes.byref(st), L, Hkv, Hq, d, capacity, sinks, _i32_array(budgets),

@@ -850,13 +850,17 @@ kvc_status kvc_layer_budgets(const float* sens, int32_t L, double alpha, int64_t
 kvc_status kvc_block_state_init(kvc_block_state* st, int32_t L, int32_t Hkv, int32_t Hq, int32_t d, int32_t capacity,
                                 int32_t sinks, const int32_t* budgets, void* K0, void* V0, int32_t* pos0, void* K1,
                                 void* V1, int32_t* pos1) {
+  // no second slab: the kept rows stay in place (one slab)
+  const bool in_place = !K1 && !V1 && !pos1;
   if (!st || !budgets || L < 1 || L > kMaxLayers || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || d != kHeadDim ||
-      sinks < 0 || capacity < 1 || !K0 || !V0 || !pos0 || !K1 || !V1 || !pos1 || !aligned16(K0) ||
-      !aligned16(V0) || !aligned16(K1) || !aligned16(V1))
+      sinks < 0 || capacity < 1 || !K0 || !V0 || !pos0 || !aligned16(K0) || !aligned16(V0))
     return KVC_ERR_INVALID;
+  if (!in_place && (!K1 || !V1 || !pos1 || !aligned16(K1) || !aligned16(V1))) return KVC_ERR_INVALID;
   // key slabs are tensor-map sources; the rest is read and written in place
-  if (!is_device_memory(K0) || !is_device_memory(K1) || !reachable(V0, V1, pos0, pos1)) return KVC_ERR_INVALID;
+  if (!is_device_memory(K0) || (K1 && !is_device_memory(K1)) || !reachable(V0, V1, pos0, pos1))
+    return KVC_ERR_INVALID;
   if (static_cast<int64_t>(L) * Hq * capacity >= (int64_t(1) << 31)) return KVC_ERR_INVALID;
+  if (in_place && (capacity > kEvictInPlaceRows || Hkv > 65535)) return KVC_ERR_INVALID;
   for (int l = 0; l < L; ++l)
     if (budgets[l] < sinks || budgets[l] > capacity) return KVC_ERR_INVALID;
   memset(st, 0, sizeof(*st));
@@ -896,7 +900,8 @@ BlockWorkspace carve_block(const kvc_block_state* st, int32_t P, void* base, siz
   for (int l = 0; l < st->L; ++l) kmax = std::max(kmax, st->budget[l]);
   const int G = st->Hq / st->Hkv;
   w.score = c.take<float>(LH * st->capacity);
-  w.kept = c.take<int32_t>(LH * kmax);
+  // kept indices, or (one slab) the hole and mover lists of each (l, h)
+  w.kept = c.take<int32_t>(LH * kmax * (st->K[1] ? 1 : 2));
   w.rw.Rpad = recon_rows(G, 1, P, P);
   w.rw.Qg = c.take<uint16_t>(LH * w.rw.Rpad * kHeadDim);
   w.rw.Kg = nullptr;
@@ -1005,11 +1010,24 @@ kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk, const v
       ep.out_off[l] = static_cast<int64_t>(l) * Hkv * kmax;
       ep.active[l] = 1;
     }
-    // eviction and compaction in one launch: each active layer's kept rows
-    // (with their global positions) move into its other slab
     EvictCopy cp;
     memset(&cp, 0, sizeof(cp));
-    for (int from = 0; from < 2; ++from) {
+    if (!st->K[1]) {
+      // one slab: kept rows stay where they are; kept block rows move into
+      // the rows of evicted ones
+      cp.K[0] = st->K[0];
+      cp.V[0] = st->V[0];
+      cp.pos[0] = st->pos[0];
+      cp.Kd[0] = st->K[0];
+      cp.Vd[0] = st->V[0];
+      cp.posd[0] = st->pos[0];
+      cp.src_ld = st->capacity;
+      cp.dst_ld = st->capacity;
+      if (launch_evict_in_place(w.score, ep, w.kept, kmax, cp, cst) != cudaSuccess) return KVC_ERR_CUDA;
+    }
+    // two slabs: eviction and compaction in one launch; each active layer's
+    // kept rows (with their global positions) move into its other slab
+    for (int from = 0; from < 2 && st->K[1]; ++from) {
       cp.K[from] = st->K[from];
       cp.V[from] = st->V[from];
       cp.pos[from] = st->pos[from];
@@ -1020,14 +1038,14 @@ kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk, const v
     cp.src_ld = st->capacity;
     cp.dst_ld = st->capacity;
     for (int l = 0; l < L; ++l) cp.slab[l] = st->cur[l];
-    if (launch_evict(w.score, ep, w.kept, nullptr, false, &cp, cst) != cudaSuccess) return KVC_ERR_CUDA;
+    if (st->K[1] && launch_evict(w.score, ep, w.kept, nullptr, false, &cp, cst) != cudaSuccess) return KVC_ERR_CUDA;
   }
   // 3. host bookkeeping
   for (int l = 0; l < L; ++l) {
     const bool active = n_now[l] > st->budget[l] && n_now[l] > st->sinks;
     if (active) {
       st->len[l] = st->budget[l];
-      st->cur[l] ^= 1;
+      if (st->K[1]) st->cur[l] ^= 1;
     } else {
       st->len[l] = n_now[l];
     }
@@ -1176,6 +1194,8 @@ kvc_status kvc_episode_pack(const kvc_block_state* st, void* Kp, void* Vp, int32
   pp.L = st->L;
   pp.Hkv = st->Hkv;
   pp.cap = st->capacity;
+  pp.ordered = st->K[1] ? 0 : 1;
+  pp.npos = st->consumed;
   int64_t row = 0;
   for (int l = 0; l < st->L; ++l) {
     if (st->len[l] < 0 || st->len[l] > st->capacity || (st->cur[l] != 0 && st->cur[l] != 1)) return KVC_ERR_INVALID;

@@ -159,6 +159,16 @@ cudaError_t launch_evict(float* score, const EvictParams& ep, int32_t* kept, uin
 // compaction launch after it (a row's copy would otherwise fall to a
 // single CTA).
 constexpr int kFusedCopyRows = 4096;
+// Eviction in place (one launch): the kept rows of every active layer end up
+// in rows [0, k_l) of slab 0 (copy.K[0] / V[0] / pos[0], written through
+// Kd[0] / Vd[0] / posd[0], the same buffers), in no particular order: each
+// kept row at or above k_l moves into an evicted row below it.  A tie at the
+// threshold goes to the lower global position (copy.pos[0]).  lists holds
+// 2 * list_stride int32 per (l, h) (list_stride >= max k_l).  Rows must fit
+// the shared-memory parts (at most kEvictInPlaceRows candidates).
+cudaError_t launch_evict_in_place(const float* score, const EvictParams& ep, int32_t* lists, int list_stride,
+                                  const EvictCopy& copy, cudaStream_t st);
+constexpr int kEvictInPlaceRows = 8 * 49152;
 
 // Compaction: dst row (l, h, t) = src row (l, h, idx[l][h][t]).
 struct CompactParams {
@@ -273,6 +283,8 @@ struct PackParams {
   int32_t len[kMaxLayers];
   int32_t cur[kMaxLayers];
   int64_t dst_off[kMaxLayers];    // first packed row of layer l
+  int ordered;                    // 1: rows in no order (one slab); pack them by ascending position
+  int64_t npos;                   // positions lie in [0, npos)
 };
 // Q4 codec of bf16 rows of 128 values (codes [rows][64] bytes, params
 // [rows][2] x (step, offset) bf16).

@@ -57,9 +57,10 @@ constexpr int CW = CT / 32;           // warps per CTA
 constexpr int kPartKeys = 16384;      // keys per CTA in the common case (64 KB)
 constexpr int kPartKeysMax = 49152;   // keys per CTA at most (192 KB)
 constexpr int kMaxParts = 8;          // CTAs per row (portable cluster size)
+static_assert(kEvictInPlaceRows == kMaxParts * kPartKeysMax, "in-place rows fit the shared-memory parts");
 
 struct TopkArgs {
-  int mode;                 // 0: per-chunk selection over p; 1: eviction over score rows
+  int mode;                 // 0: per-chunk selection over p; 1: eviction over score rows; 2: eviction in place
   const float* vals;        // p (mode 0) or score (mode 1)
   // mode 0
   int N, sinks, m, n_chunks, nq_full, nq_last;
@@ -71,19 +72,22 @@ struct TopkArgs {
   uint32_t* gmax;           // [0] max order key, [1] arrivals; null: no pin
   int total_ctas;           // CTAs of the launch (last-arriver pin)
   int copy;                 // fused compaction of the kept rows
+  int fill;                 // mode 2: entries per (l, h) of each pair list (holes, then movers)
+  int* status;              // mode 2: KVC bounds status if holes and movers ever disagree
 };
 
 struct TopkShared {
   uint32_t whist[CW][256];  // per-warp histograms of one digit
   uint32_t chist[2][256];   // this CTA's histogram by pass parity (read by the cluster)
   uint32_t ghist[256];      // the cluster's histogram of the current digit
-  uint32_t xch[4];          // min key, max key, gt count, eq count (read by the cluster)
+  uint32_t xch[6];          // min key, max key, gt count, eq count, holes, movers (read by the cluster)
   uint32_t wgt[CW], weq[CW];
   uint32_t wsel[CW], weqb[CW];  // per warp: first output slot, global eq rank of its first key
   uint32_t kmin, kmax;      // the cluster's candidate range
   uint32_t digit, rem;
   uint32_t lmin, lmax;      // this CTA's
   uint32_t sel_cta, sel_before;
+  uint32_t eq_total;        // keys == T in the whole row
   int last;
 };
 
@@ -128,6 +132,87 @@ __device__ __forceinline__ void csync(cg::cluster_group& cl) {
     cl.sync();
   else
     __syncthreads();
+}
+
+// MSB-first radix select over the cluster's staged keys: the need-th
+// largest key T (every key of the cluster lies in [kmin, kmax]) and how many
+// keys == T are taken.  Digits of 8 bits below the common prefix of kmin and
+// kmax; per-warp histograms, summed per CTA and then over the cluster in rank
+// order through distributed shared memory, so every CTA finds the same digit.
+// Requires 1 <= need < number of keys.
+template <bool MULTI>
+__device__ void radix_select(cg::cluster_group& cl, TopkShared& sm, const uint32_t* keys, int cnt, int C,
+                             uint32_t need, uint32_t kmin, uint32_t kmax, uint32_t& T, uint32_t& eq_need) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t diff = kmin ^ kmax;
+  int hb = diff ? 32 - __clz(diff) : 0;           // bits below the common prefix
+  uint32_t prefix = hb >= 32 ? 0u : (kmax & ~((1u << hb) - 1u));
+  uint32_t rem = need;
+  int par = 0;
+  while (hb > 0) {
+    const int lb = max(hb - 8, 0);
+    const uint32_t pmask = hb >= 32 ? 0u : (~0u << hb);
+    const uint32_t dmask = (1u << (hb - lb)) - 1u;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) sm.whist[warp][lane * 8 + t] = 0u;
+    __syncwarp();
+    for (int j = tid; j < cnt; j += CT) {
+      const uint32_t k = keys[j];
+      if ((k & pmask) == prefix) atomicAdd(&sm.whist[warp][(k >> lb) & dmask], 1u);
+    }
+    __syncthreads();
+    if (tid < 256) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < CW; ++w) t += sm.whist[w][tid];
+      sm.chist[par][tid] = t;
+    }
+    const uint32_t* H = sm.chist[par];
+    if (MULTI) {
+      cl.sync();
+      if (tid < 256) {
+        uint32_t t = 0;
+        for (int r = 0; r < C; ++r) t += cl.map_shared_rank(sm.chist[par], r)[tid];
+        sm.ghist[tid] = t;
+      }
+      H = sm.ghist;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // bins from the top: lane l covers bins 255-8l .. 248-8l
+      uint32_t c[8], tot = 0;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        c[t] = H[255 - (lane * 8 + t)];
+        tot += c[t];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const uint32_t excl = incl - tot;
+      if (excl < rem && incl >= rem) {
+        uint32_t run = excl;
+        for (int t = 0; t < 8; ++t) {
+          if (run + c[t] >= rem) {
+            sm.digit = 255u - (lane * 8 + t);
+            sm.rem = rem - run;
+            break;
+          }
+          run += c[t];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= sm.digit << lb;
+    rem = sm.rem;
+    hb = lb;
+    par ^= 1;
+  }
+  T = prefix;
+  eq_need = rem;
 }
 
 // Copy the kept rows t in [t0, t1) of (l, h) from the source slab into the
@@ -178,7 +263,160 @@ __device__ void copy_rows(const EvictParams& P, const EvictCopy& X, int l, int h
   }
 }
 
+// Row moves of an in-place eviction: rows movers[i] -> holes[i] for i in
+// [p0, p1) of (l, h), K and V (and positions) in slab 0.  Holes lie below the
+// budget and movers at or above it, so no row is both read and written.
+// K and V rows form one stream of 256-byte row copies, half a warp per row,
+// eight in flight per half-warp.
+__device__ void move_rows(const EvictCopy& X, int64_t lh, const int32_t* holes, const int32_t* movers, int p0,
+                          int p1) {
+  uint4* K = static_cast<uint4*>(X.Kd[0]);
+  uint4* V = static_cast<uint4*>(X.Vd[0]);
+  int32_t* pos = X.posd[0];
+  const int64_t base = lh * X.src_ld;
+  const int sub = threadIdx.x & 15, hw = threadIdx.x >> 4;
+  constexpr int HW = CT / 16;
+  constexpr int R = 8;
+  const int np = p1 - p0;
+  const int total = 2 * np;             // K rows, then V rows
+  for (int ub = hw; ub < total; ub += HW * R) {
+    int32_t src[R];
+    uint4 val[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      const int w = ub + u * HW;
+      src[u] = -1;
+      if (w < total) {
+        src[u] = movers[p0 + (w < np ? w : w - np)];
+        val[u] = (w < np ? K : V)[(base + src[u]) * 16 + sub];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      const int w = ub + u * HW;
+      if (src[u] < 0) continue;
+      const bool isK = w < np;
+      const int dst = holes[p0 + (isK ? w : w - np)];
+      (isK ? K : V)[(base + dst) * 16 + sub] = val[u];
+      if (isK && sub == 0) pos[base + dst] = pos[base + src[u]];
+    }
+  }
+}
+
+// Eviction in place (mode 2): the kept rows of (l, h) end up in rows [0, k)
+// of slab 0 in no particular order.  A kept row at or above k (a "mover")
+// moves into an evicted row below k (a "hole"); the i-th hole in row order
+// takes the i-th mover, and there are as many of each.  Rows carry their
+// global position (X.pos[0]), and a tie at the threshold is decided by it,
+// lower position first, as in the ascending layout where row order is
+// position order.
 template <bool MULTI>
+__device__ void evict_in_place(cg::cluster_group& cl, TopkShared& sm, uint32_t* keys, int cnt, int C, int rank,
+                               const RowDesc& R, const TopkArgs& A, const EvictParams& P, const EvictCopy& X,
+                               uint32_t T, uint32_t eq_need, int c0, int wb0, int wb1) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t lt = (1u << lane) - 1u;
+  const int64_t lh = static_cast<int64_t>(R.l) * P.Hkv + R.h;
+  // a. more keys == T than are kept: rank them by position.  New keys: every
+  // key > T above every tie, ties ordered by lower position (all distinct),
+  // the rest at 0; the need-th largest of them is the new threshold and it
+  // has no ties.
+  if (sm.eq_total > eq_need) {
+    const int32_t* pos = X.pos[0] + lh * X.src_ld + c0;
+    for (int j = tid; j < cnt; j += CT) {
+      const uint32_t k = keys[j];
+      keys[j] = k > T ? 0xffffffffu : (k == T ? 0x80000000u - static_cast<uint32_t>(pos[j]) : 0u);
+    }
+    __syncthreads();
+    uint32_t one;
+    radix_select<MULTI>(cl, sm, keys, cnt, C, R.need, 0u, 0xffffffffu, T, one);
+  }
+  // every key >= T is kept now
+  // b. holes and movers per warp block, then their ranks across the row
+  const int kb = P.k[R.l];
+  {
+    uint32_t nh = 0, nm = 0;
+    for (int jb = wb0; jb < wb1; jb += 32) {
+      const int j = jb + lane;
+      const bool in = j < wb1;
+      const bool take = in && keys[j] >= T;
+      nh += __popc(__ballot_sync(0xffffffffu, in && !take && c0 + j < kb));
+      nm += __popc(__ballot_sync(0xffffffffu, take && c0 + j >= kb));
+    }
+    if (lane == 0) {
+      sm.wgt[warp] = nh;
+      sm.weq[warp] = nm;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t h = 0, m = 0;
+    for (int w = 0; w < CW; ++w) {
+      h += sm.wgt[w];
+      m += sm.weq[w];
+    }
+    sm.xch[4] = h;
+    sm.xch[5] = m;
+  }
+  csync<MULTI>(cl);
+  if (tid == 0) {
+    uint32_t hb = 0, mb = 0, ht = 0, mt = 0;
+    for (int r = 0; r < C; ++r) {
+      const uint32_t* x = MULTI ? cl.map_shared_rank(sm.xch, r) : sm.xch;
+      if (r < rank) {
+        hb += x[4];
+        mb += x[5];
+      }
+      ht += x[4];
+      mt += x[5];
+    }
+    for (int w = 0; w < CW; ++w) {
+      sm.wsel[w] = hb;
+      sm.weqb[w] = mb;
+      hb += sm.wgt[w];
+      mb += sm.weq[w];
+    }
+    // equal by construction (exactly need keys are kept); only the pairs
+    // both lists hold are moved
+    sm.sel_cta = min(min(ht, mt), static_cast<uint32_t>(A.fill));
+    if ((ht != mt || mt > static_cast<uint32_t>(A.fill)) && rank == 0 && A.status)
+      record_status(A.status, DEV_BOUNDS);
+  }
+  __syncthreads();
+  int32_t* holes = A.kept + lh * 2 * A.fill;
+  int32_t* movers = holes + A.fill;
+  {
+    uint32_t hr = sm.wsel[warp], mr = sm.weqb[warp];
+    for (int jb = wb0; jb < wb1; jb += 32) {
+      const int j = jb + lane;
+      const bool in = j < wb1;
+      const bool take = in && keys[j] >= T;
+      const bool ho = in && !take && c0 + j < kb;
+      const bool mo = take && c0 + j >= kb;
+      const uint32_t hm = __ballot_sync(0xffffffffu, ho);
+      const uint32_t mm = __ballot_sync(0xffffffffu, mo);
+      const uint32_t hi = hr + __popc(hm & lt), mi = mr + __popc(mm & lt);
+      if (ho && hi < static_cast<uint32_t>(A.fill)) holes[hi] = c0 + j;
+      if (mo && mi < static_cast<uint32_t>(A.fill)) movers[mi] = c0 + j;
+      hr += __popc(hm);
+      mr += __popc(mm);
+    }
+  }
+  // the lists are complete (and no peer reads this CTA's shared memory
+  // after this point)
+  __threadfence();
+  if (MULTI) cl.sync();
+  else __syncthreads();
+  // c. this CTA's share of the pairs
+  const int np = static_cast<int>(sm.sel_cta);
+  const int per = (np + C - 1) / C;
+  const int p0 = min(rank * per, np), p1 = min(p0 + per, np);
+  move_rows(X, lh, holes, movers, p0, p1);
+}
+
+// INPLACE: the in-place eviction (mode 2) only; a separate instance keeps
+// its registers out of the other modes.
+template <bool MULTI, bool INPLACE>
 __global__ void __launch_bounds__(CT, 2)
     topk_cluster_kernel(const __grid_constant__ TopkArgs A, const __grid_constant__ EvictParams P,
                         const __grid_constant__ EvictCopy X) {
@@ -257,76 +495,7 @@ __global__ void __launch_bounds__(CT, 2)
     T = 0u;                   // every key is >= 0: keep all
     eq_need = 0xffffffffu;
   } else {
-    const uint32_t kmin = sm.kmin, kmax = sm.kmax;
-    const uint32_t diff = kmin ^ kmax;
-    int hb = diff ? 32 - __clz(diff) : 0;           // bits below the common prefix
-    uint32_t prefix = hb >= 32 ? 0u : (kmax & ~((1u << hb) - 1u));
-    uint32_t rem = R.need;
-    int par = 0;
-    while (hb > 0) {
-      const int lb = max(hb - 8, 0);
-      const uint32_t pmask = hb >= 32 ? 0u : (~0u << hb);
-      const uint32_t dmask = (1u << (hb - lb)) - 1u;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) sm.whist[warp][lane * 8 + t] = 0u;
-      __syncwarp();
-      for (int j = tid; j < cnt; j += CT) {
-        const uint32_t k = keys[j];
-        if ((k & pmask) == prefix) atomicAdd(&sm.whist[warp][(k >> lb) & dmask], 1u);
-      }
-      __syncthreads();
-      if (tid < 256) {
-        uint32_t t = 0;
-#pragma unroll
-        for (int w = 0; w < CW; ++w) t += sm.whist[w][tid];
-        sm.chist[par][tid] = t;
-      }
-      const uint32_t* H = sm.chist[par];
-      if (MULTI) {
-        cl.sync();
-        if (tid < 256) {
-          uint32_t t = 0;
-          for (int r = 0; r < C; ++r) t += cl.map_shared_rank(sm.chist[par], r)[tid];
-          sm.ghist[tid] = t;
-        }
-        H = sm.ghist;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        // bins from the top: lane l covers bins 255-8l .. 248-8l
-        uint32_t c[8], tot = 0;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          c[t] = H[255 - (lane * 8 + t)];
-          tot += c[t];
-        }
-        uint32_t incl = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const uint32_t excl = incl - tot;
-        if (excl < rem && incl >= rem) {
-          uint32_t run = excl;
-          for (int t = 0; t < 8; ++t) {
-            if (run + c[t] >= rem) {
-              sm.digit = 255u - (lane * 8 + t);
-              sm.rem = rem - run;
-              break;
-            }
-            run += c[t];
-          }
-        }
-      }
-      __syncthreads();
-      prefix |= sm.digit << lb;
-      rem = sm.rem;
-      hb = lb;
-      par ^= 1;
-    }
-    T = prefix;
-    eq_need = rem;
+    radix_select<MULTI>(cl, sm, keys, cnt, C, R.need, sm.kmin, sm.kmax, T, eq_need);
   }
 
   // ---- 3. counts per warp block (contiguous, whole multiples of 32 keys)
@@ -359,13 +528,16 @@ __global__ void __launch_bounds__(CT, 2)
   csync<MULTI>(cl);
   if (tid == 0) {
     // keys == T are taken in position order across the cluster, then the CTA
-    uint32_t sel_before = 0, eq_before = 0;
-    for (int r = 0; r < rank; ++r) {
+    uint32_t sel_before = 0, eq_before = 0, eq_total = 0;
+    for (int r = 0; r < C; ++r) {
       const uint32_t* x = MULTI ? cl.map_shared_rank(sm.xch, r) : sm.xch;
+      eq_total += x[3];
+      if (r >= rank) continue;
       const uint32_t take = eq_need > eq_before ? min(eq_need - eq_before, x[3]) : 0u;
       sel_before += x[2] + take;
       eq_before += x[3];
     }
+    sm.eq_total = eq_total;
     uint32_t s = sel_before;
     for (int w = 0; w < CW; ++w) {
       sm.wsel[w] = s;
@@ -378,6 +550,10 @@ __global__ void __launch_bounds__(CT, 2)
     sm.sel_cta = s - sel_before;
   }
   __syncthreads();
+  if (INPLACE) {
+    evict_in_place<MULTI>(cl, sm, keys, cnt, C, rank, R, A, P, X, T, eq_need, c0, wb0, wb1);
+    return;
+  }
 
   // ---- 4. ordered emit; for the fused copy the CTA's positions are also
   // kept in shared memory (in the histogram area, free by now) when they fit
@@ -680,22 +856,23 @@ cudaError_t launch_cluster(const TopkArgs& A, const EvictParams& P, const EvictC
   // Two CTAs of a 64 KB part share an SM only with the largest shared-memory
   // carveout.  Attributes are set once per device (for the largest part size),
   // not on every launch.
-  static int attr_done[64][2];
+  static int attr_done[64][4];
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return cudaErrorInvalidDevice;
-  const int multi = parts > 1 ? 1 : 0;
-  if (!attr_done[d][multi]) {
-    const void* fn = multi ? reinterpret_cast<const void*>(topk_cluster_kernel<true>)
-                           : reinterpret_cast<const void*>(topk_cluster_kernel<false>);
+  const int variant = (parts > 1 ? 1 : 0) + (A.mode == 2 ? 2 : 0);
+  void (*const fns[4])(TopkArgs, EvictParams, EvictCopy) = {
+      topk_cluster_kernel<false, false>, topk_cluster_kernel<true, false>, topk_cluster_kernel<false, true>,
+      topk_cluster_kernel<true, true>};
+  if (!attr_done[d][variant]) {
+    const void* fn = reinterpret_cast<const void*>(fns[variant]);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kPartKeysMax * sizeof(uint32_t)));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr_done[d][multi] = 1;
+    attr_done[d][variant] = 1;
   }
-  if (multi) return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, A, P, X);
-  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, A, P, X);
+  return cudaLaunchKernelEx(&cfg, fns[variant], A, P, X);
 }
 
 // Largest order key over the non-sink entries of LH rows of N scores.
@@ -831,6 +1008,33 @@ cudaError_t launch_evict(float* score, const EvictParams& ep, int32_t* kept, uin
   }
   if (!copy) return cudaSuccess;
   return compact_after(ep, kept, *copy, st);
+}
+
+
+cudaError_t launch_evict_in_place(const float* score, const EvictParams& ep, int32_t* lists, int list_stride,
+                                  const EvictCopy& copy, cudaStream_t st) {
+  TopkArgs A;
+  memset(&A, 0, sizeof(A));
+  int n_act = 0;
+  int64_t longest = 0;
+  for (int l = 0; l < ep.L; ++l) {
+    if (!ep.active[l]) continue;
+    A.act[n_act++] = l;
+    longest = std::max<int64_t>(longest, static_cast<int64_t>(ep.n[l]) - ep.sinks);
+  }
+  if (n_act == 0) return cudaSuccess;
+  int parts = 1, part_keys = 4;
+  if (ep.Hkv > 65535 || !plan_parts(longest, &parts, &part_keys)) return cudaErrorInvalidValue;
+  A.mode = 2;
+  A.vals = score;
+  A.kept = lists;
+  A.fill = list_stride;
+  A.status = status_word();
+  A.total_ctas = parts * ep.Hkv * n_act;
+  ProfScope ps("evict_in_place", st);
+  cudaError_t e = launch_cluster(A, ep, copy, parts, part_keys, dim3(parts, ep.Hkv, n_act), st);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace kvc

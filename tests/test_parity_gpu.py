@@ -457,14 +457,31 @@ def test_tiny_unchained_pipeline(qk):
     print(f"tiny-4k: {diff} kept positions differ from the oracle's own pipeline")
 
 
+def _block_state(qk, L, H, Hq, cap, S, budgets, layout):
+    """Block-prefill state in the two-slab or one-slab layout; returns the
+    state, the K/V slabs [K0, V0, (K1, V1)] and the position arrays."""
+    n_slab = 2 if layout == "two-slab" else 1
+    slabs = [torch.zeros(L * H * cap * 128, dtype=torch.bfloat16, device=DEV) for _ in range(2 * n_slab)]
+    pos = [torch.zeros(L * H * cap, dtype=torch.int32, device=DEV) for _ in range(n_slab)]
+    if n_slab == 2:
+        st = qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0], slabs[2], slabs[3],
+                                     pos[1])
+    else:
+        st = qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0])
+    return st, slabs, pos
+
+
+@pytest.mark.parametrize("layout", ["two-slab", "one-slab"])
 @pytest.mark.parametrize("name", list(EPI_CASES))
-def test_block_prefill_matches_oracle(qk, name):
+def test_block_prefill_matches_oracle(qk, name, layout):
     """EpiCache-style streaming with per-layer budgets, small shapes, checked
     step by step: every over-budget step of every layer is compared with one
-    oracle step started from the GPU's state before it -- the step's scores
-    element-wise (1e-3 relative, read from the workspace), the kept set up to
-    oracle near-ties within 1e-4 of the threshold, the kept K and V rows bit
-    for bit; an under-budget step must append the block unchanged."""
+    oracle step started from the GPU's state before it, in ascending position
+    order -- the step's scores element-wise (1e-3 relative, read from the
+    workspace), the kept set up to oracle near-ties within 1e-4 of the
+    threshold, the kept K and V rows bit for bit; an under-budget step must
+    append the block unchanged.  The one-slab layout holds the same rows in
+    another order; its packed image must be in position order."""
     case = dict(n_hist=1500, block=256)
     case.update(EPI_CASES[name])
     cfg = ks.EpiConfig(name, d=128, episodes=1, prompt_len=24, alpha=3.0, sinks=4, **case)
@@ -477,9 +494,7 @@ def test_block_prefill_matches_oracle(qk, name):
     prm = [ks.gen_epi_prompt_layer(cfg, 0, l) for l in range(L)]
     Qp = np.stack([p[0] for p in prm]); Kp = np.stack([p[1] for p in prm])
     cap = max(budgets) + B
-    slabs = [torch.zeros(L * H * cap * 128, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
-    pos = [torch.zeros(L * H * cap, dtype=torch.int32, device=DEV) for _ in range(2)]
-    st = qk.kvc_block_state_init(L, H, Hq, cap, S, budgets, slabs[0], slabs[1], pos[0], slabs[2], slabs[3], pos[1])
+    st, slabs, pos = _block_state(qk, L, H, Hq, cap, S, budgets, layout)
     ws = torch.empty(qk.kvc_block_workspace_size(st, B, P), dtype=torch.uint8, device=DEV)
     Qp_d, Kp_d = to_dev(Qp), to_dev(Kp)
     Kf = [kv2.bf16_to_f64(Kh[l]) for l in range(L)]
@@ -505,17 +520,25 @@ def test_block_prefill_matches_oracle(qk, name):
             for h in range(H):
                 np.testing.assert_array_equal(got_K[h], Kh[l, h][got_pos[h]])
                 np.testing.assert_array_equal(got_V[h], Vh[l, h][got_pos[h]])
+            if layout == "two-slab":
+                assert np.all(np.diff(got_pos, axis=1) > 0), (t0, l)
             if n_cat <= budgets[l]:
                 assert np.array_equal(got_pos, cat_pos), (t0, l)
                 continue
-            # one oracle step from the GPU's previous state
-            Kcat = np.stack([Kf[l][h][cat_pos[h]] for h in range(H)])
+            # one oracle step from the GPU's previous state, in position order
+            # (the GPU scored its rows in row order: order maps one to the other)
+            order = np.argsort(cat_pos, axis=1, kind="stable")
+            cat_sorted = np.take_along_axis(cat_pos, order, axis=1)
+            assert np.all(cat_sorted[:, :S] == np.arange(S)), "sinks first in both orders"
+            Kcat = np.stack([Kf[l][h][cat_sorted[h]] for h in range(H)])
             sc = kv2.block_step_scores(Kcat, Qf[l], Kpf[l], S)
             for h in range(H):
-                compare.assert_scores(step_scores[l, h, S:n_cat], sc[h, S:], floor=0.0,
+                compare.assert_scores(step_scores[l, h, :n_cat][order[h]][S:], sc[h, S:], floor=0.0,
                                       what=f"block {t0} layer {l} head {h} scores")
-                idx = np.searchsorted(cat_pos[h], got_pos[h])
-                assert np.array_equal(cat_pos[h][idx], got_pos[h])
+                kept_sorted = np.sort(got_pos[h])
+                assert len(np.unique(kept_sorted)) == len(kept_sorted)
+                idx = np.searchsorted(cat_sorted[h], kept_sorted)
+                assert np.array_equal(cat_sorted[h][idx], kept_sorted)
                 compare.assert_topk_set(idx, sc[h], S, n_cat, budgets[l] - S, forced=range(S),
                                         what=f"block {t0} layer {l} head {h} kept")
             scored += 1
@@ -526,7 +549,84 @@ def test_block_prefill_matches_oracle(qk, name):
         ref = kv2.block_prefill_layer(Kf[l], kv2.bf16_to_f64(Vh[l]), Qf[l], Kpf[l], B, budgets[l], S)
         got = pos[st.cur[l]].view(L, H, cap)[l, :, :st.len[l]].cpu().numpy()
         diff += sum(len(set(got[h].tolist()) ^ set(ref[2][h].tolist())) for h in range(H))
-    print(f"{name}: {scored} scored layer steps; {diff} positions differ from the unchained oracle")
+    print(f"{name} ({layout}): {scored} scored layer steps; {diff} positions differ from the unchained oracle")
+    # the packed image: every segment in ascending position order
+    R = qk.kvc_episode_rows(st)
+    Kpk = torch.empty(R * 128, dtype=torch.bfloat16, device=DEV)
+    Vpk = torch.empty_like(Kpk)
+    ppk = torch.empty(R, dtype=torch.int32, device=DEV)
+    qk.kvc_episode_pack(st, Kpk, Vpk, ppk)
+    assert qk.kvc_stream_status() == 0
+    Kb_, Vb_, pb_ = bits_of(Kpk).reshape(R, 128), bits_of(Vpk).reshape(R, 128), ppk.cpu().numpy()
+    row = 0
+    for l in range(L):
+        n = st.len[l]
+        got = pos[st.cur[l]].view(L, H, cap)[l, :, :n].cpu().numpy()
+        for h in range(H):
+            want = np.sort(got[h])
+            np.testing.assert_array_equal(pb_[row:row + n], want)
+            np.testing.assert_array_equal(Kb_[row:row + n], Kh[l, h][want])
+            np.testing.assert_array_equal(Vb_[row:row + n], Vh[l, h][want])
+            row += n
+    assert row == R
+
+
+def test_block_prefill_one_slab_ties(qk):
+    """Exact score ties: history keys drawn from 24 distinct rows, so rows
+    with the same key score the same and the threshold falls inside groups of
+    equal scores.  The one-slab layout, whose rows are not in position order,
+    must keep the same positions as the two-slab layout (lower global position
+    wins a tie) at every step."""
+    cfg = ks.EpiConfig("epi-ties", L=3, Hkv=2, Hq=6, d=128, n_hist=1500, block=256, episodes=1, prompt_len=24,
+                       mean_budget=300, alpha=3.0, sinks=4)
+    sens = ks.gen_sensitivity(cfg)
+    budgets = qk.kvc_layer_budgets(sens.tolist(), cfg.alpha, cfg.mean_budget, cfg.sinks)
+    L, H, Hq, B, P, S = cfg.L, cfg.Hkv, cfg.Hq, cfg.block, cfg.prompt_len, cfg.sinks
+    rng = np.random.default_rng(7)
+    pool = ks.gen_epi_history_layer(cfg, 0)[0][0, :24]                       # 24 distinct bf16 key rows
+    Kh = pool[rng.integers(0, 24, size=(L, H, cfg.n_hist))]
+    Vh = np.stack([ks.gen_epi_history_layer(cfg, l)[1] for l in range(L)])
+    prm = [ks.gen_epi_prompt_layer(cfg, 0, l) for l in range(L)]
+    Qp_d = to_dev(np.stack([p[0] for p in prm]))
+    Kp_d = to_dev(np.stack([p[1] for p in prm]))
+    cap = max(budgets) + B
+    runs = [_block_state(qk, L, H, Hq, cap, S, budgets, lay) for lay in ("two-slab", "one-slab")]
+    wss = [torch.empty(qk.kvc_block_workspace_size(r[0], B, P), dtype=torch.uint8, device=DEV) for r in runs]
+    tied = 0
+    for t0 in range(0, cfg.n_hist, B):
+        t1 = min(t0 + B, cfg.n_hist)
+        st0, _, pos0 = runs[0]
+        prev = [pos0[st0.cur[l]].view(L, H, cap)[l, :, :st0.len[l]].cpu().numpy() for l in range(L)]
+        kb = to_dev(np.ascontiguousarray(Kh[:, :, t0:t1]))
+        vb = to_dev(np.ascontiguousarray(Vh[:, :, t0:t1]))
+        sets = []
+        for (st, slabs, pos), ws in zip(runs, wss):
+            qk.kvc_block_prefill_step(st, kb, vb, t1 - t0, Qp_d, Kp_d, P, ws=ws)
+            assert qk.kvc_stream_status() == 0
+            sets.append([pos[st.cur[l]].view(L, H, cap)[l, :, :st.len[l]].cpu().numpy() for l in range(L)])
+            for l in range(L):
+                Kg = bits_of(slabs[2 * st.cur[l]]).reshape(L, H, cap, 128)[l, :, :st.len[l]]
+                Vg = bits_of(slabs[2 * st.cur[l] + 1]).reshape(L, H, cap, 128)[l, :, :st.len[l]]
+                for h in range(H):
+                    np.testing.assert_array_equal(Kg[h], Kh[l, h][sets[-1][l][h]])
+                    np.testing.assert_array_equal(Vg[h], Vh[l, h][sets[-1][l][h]])
+        sc = wss[0][:L * H * cap * 4].view(torch.float32).cpu().numpy().reshape(L, H, cap)
+        for l in range(L):
+            n_cat = prev[l].shape[1] + t1 - t0
+            for h in range(H):
+                assert np.array_equal(np.sort(sets[1][l][h]), sets[0][l][h]), (t0, l, h)
+            if n_cat <= budgets[l]:
+                continue
+            for h in range(H):
+                # a tie at the threshold: a score value both kept and evicted
+                cat = np.concatenate([prev[l][h], np.arange(t0, t1)])
+                keep = np.isin(cat, sets[0][l][h])
+                keep[:S] = False
+                thr = sc[l, h, :n_cat][keep].min()
+                out = ~np.isin(cat, sets[0][l][h])
+                tied += int(np.any(sc[l, h, :n_cat][out] == thr))
+    assert tied > 0, "the case must exercise ties at the threshold"
+    print(f"{tied} (step, layer, head) evictions had ties at the threshold")
 
 
 @pytest.mark.slow
