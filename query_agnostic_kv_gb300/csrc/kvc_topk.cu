@@ -83,6 +83,7 @@ struct TopkShared {
   uint32_t xch[6];          // min key, max key, gt count, eq count, holes, movers (read by the cluster)
   uint32_t wgt[CW], weq[CW];
   uint32_t wsel[CW], weqb[CW];  // per warp: first output slot, global eq rank of its first key
+  uint32_t whol[CW], wmov[CW];  // in-place eviction, per warp: holes and movers
   uint32_t kmin, kmax;      // the cluster's candidate range
   uint32_t digit, rem;
   uint32_t lmin, lmax;      // this CTA's
@@ -321,6 +322,7 @@ __device__ void evict_in_place(cg::cluster_group& cl, TopkShared& sm, uint32_t* 
   // key > T above every tie, ties ordered by lower position (all distinct),
   // the rest at 0; the need-th largest of them is the new threshold and it
   // has no ties.
+  const int kb = P.k[R.l];
   if (sm.eq_total > eq_need) {
     const int32_t* pos = X.pos[0] + lh * X.src_ld + c0;
     for (int j = tid; j < cnt; j += CT) {
@@ -330,11 +332,8 @@ __device__ void evict_in_place(cg::cluster_group& cl, TopkShared& sm, uint32_t* 
     __syncthreads();
     uint32_t one;
     radix_select<MULTI>(cl, sm, keys, cnt, C, R.need, 0u, 0xffffffffu, T, one);
-  }
-  // every key >= T is kept now
-  // b. holes and movers per warp block, then their ranks across the row
-  const int kb = P.k[R.l];
-  {
+    // the holes and movers counted with the counts assumed every tie kept:
+    // count them again
     uint32_t nh = 0, nm = 0;
     for (int jb = wb0; jb < wb1; jb += 32) {
       const int j = jb + lane;
@@ -344,21 +343,23 @@ __device__ void evict_in_place(cg::cluster_group& cl, TopkShared& sm, uint32_t* 
       nm += __popc(__ballot_sync(0xffffffffu, take && c0 + j >= kb));
     }
     if (lane == 0) {
-      sm.wgt[warp] = nh;
-      sm.weq[warp] = nm;
+      sm.whol[warp] = nh;
+      sm.wmov[warp] = nm;
     }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t h = 0, m = 0;
-    for (int w = 0; w < CW; ++w) {
-      h += sm.wgt[w];
-      m += sm.weq[w];
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t h = 0, m = 0;
+      for (int w = 0; w < CW; ++w) {
+        h += sm.whol[w];
+        m += sm.wmov[w];
+      }
+      sm.xch[4] = h;
+      sm.xch[5] = m;
     }
-    sm.xch[4] = h;
-    sm.xch[5] = m;
+    csync<MULTI>(cl);
   }
-  csync<MULTI>(cl);
+  // every key >= T is kept now
+  // b. ranks of the holes and movers across the row
   if (tid == 0) {
     uint32_t hb = 0, mb = 0, ht = 0, mt = 0;
     for (int r = 0; r < C; ++r) {
@@ -373,8 +374,8 @@ __device__ void evict_in_place(cg::cluster_group& cl, TopkShared& sm, uint32_t* 
     for (int w = 0; w < CW; ++w) {
       sm.wsel[w] = hb;
       sm.weqb[w] = mb;
-      hb += sm.wgt[w];
-      mb += sm.weq[w];
+      hb += sm.whol[w];
+      mb += sm.wmov[w];
     }
     // equal by construction (exactly need keys are kept); only the pairs
     // both lists hold are moved
@@ -502,28 +503,49 @@ __global__ void __launch_bounds__(CT, 2)
   const int WB = ((cnt + CW - 1) / CW + 31) & ~31;
   const int wb0 = min(warp * WB, cnt), wb1 = min(wb0 + WB, cnt);
   {
-    uint32_t g = 0, e = 0;
+    // the in-place eviction also counts its holes and movers, assuming every
+    // key == T is kept (true unless more keys tie at T than are kept)
+    const int kb = INPLACE ? P.k[R.l] : 0;
+    uint32_t g = 0, e = 0, nh = 0, nm = 0;
     for (int j = wb0 + lane; j < wb1; j += 32) {
       const uint32_t k = keys[j];
       g += k > T;
       e += k == T;
+      if (INPLACE) {
+        nh += (k < T && c0 + j < kb) ? 1u : 0u;
+        nm += (k >= T && c0 + j >= kb) ? 1u : 0u;
+      }
     }
     g = __reduce_add_sync(0xffffffffu, g);
     e = __reduce_add_sync(0xffffffffu, e);
+    if (INPLACE) {
+      nh = __reduce_add_sync(0xffffffffu, nh);
+      nm = __reduce_add_sync(0xffffffffu, nm);
+    }
     if (lane == 0) {
       sm.wgt[warp] = g;
       sm.weq[warp] = e;
+      if (INPLACE) {
+        sm.whol[warp] = nh;
+        sm.wmov[warp] = nm;
+      }
     }
   }
   __syncthreads();
   if (tid == 0) {
-    uint32_t g = 0, e = 0;
+    uint32_t g = 0, e = 0, h = 0, m = 0;
     for (int w = 0; w < CW; ++w) {
       g += sm.wgt[w];
       e += sm.weq[w];
+      if (INPLACE) {
+        h += sm.whol[w];
+        m += sm.wmov[w];
+      }
     }
     sm.xch[2] = g;
     sm.xch[3] = e;
+    sm.xch[4] = h;
+    sm.xch[5] = m;
   }
   csync<MULTI>(cl);
   if (tid == 0) {
