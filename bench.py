@@ -101,12 +101,13 @@ def algorithmic_work(cfg):
 
 
 # DRAM bytes per launch of the row-LSE kernel as ncu counted them (one pass,
-# no replay) on the 4-layer case of the 16K workload: dram__bytes_read +
-# dram__bytes_write = 202.27 + 3.82 MB (the writes are the 32-byte lse rows
-# the column-max pass reads, part of them still in L2 when the kernel ends);
-# the traffic grows with the number of (layer, KV head) pairs.  Reset to None
-# whenever the kernel changes until it is captured again.
-LSE_TRAFFIC_PER_LAYER = (202.27e6 + 3.82e6) / 4
+# no replay) on the 4-layer case of the 16K workload, the mean of two
+# launches: dram__bytes_read + dram__bytes_write = 202.59 + 5.69 MB (the
+# writes are the 32-byte lse rows the column-max pass reads, part of them
+# still in L2 when the kernel ends); the traffic grows with the number of
+# (layer, KV head) pairs.  Reset to None whenever the kernel changes until it
+# is captured again.
+LSE_TRAFFIC_PER_LAYER = (202.59e6 + 5.69e6) / 4
 
 
 def load_peaks():
@@ -385,9 +386,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         traffic = LSE_TRAFFIC_PER_LAYER * cfg.L
     roof = {"kernel": "recon_lse (tcgen05 row-LSE pass)", "bound": "tensor", "achieved": ach_lse,
             "peak": peak_tf, "unit": "TFLOP/s", "frac": ach_lse / peak_tf, "traffic": traffic,
-            "traffic_source": "ncu dram bytes of the 4-layer case, scaled by layers; taken before the kernel "
-                              "gained its longest-first wave order, which applies only when the active layers "
-                              "differ in length (all layers are equally long here, so the loads are unchanged)",
+            "traffic_source": "ncu dram bytes (read + write, one pass) of the 4-layer case on the current "
+                              "kernel, scaled by layers",
             "peak_source": f"bf16_tflops (burst) of {peak_src} peaks",
             "frac_of_sustained": ach_lse / peak_sus,
             "algorithmic_flops_per_launch": work["flops_lse_per_launch"],

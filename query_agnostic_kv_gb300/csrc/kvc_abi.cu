@@ -950,6 +950,12 @@ kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk, const v
   for (int l = 0; l < L; ++l) {
     ap.len[l] = st->len[l];
     ap.cur[l] = st->cur[l];
+    // one slab: a block row landing at or above the budget of a layer that
+    // evicts this step keeps its V only if it is kept, and then the eviction
+    // takes it from the block; its K is appended for the scoring
+    const int64_t n = static_cast<int64_t>(st->len[l]) + blk_len;
+    const bool evicts = n > st->budget[l] && n > st->sinks;
+    ap.vrows[l] = (!st->K[1] && evicts) ? std::max(0, st->budget[l] - st->len[l]) : blk_len;
   }
   if (launch_append(Kblk, Vblk, st->K[0], st->V[0], st->pos[0], st->K[1], st->V[1], st->pos[1], ap, cst) !=
       cudaSuccess)
@@ -1023,6 +1029,9 @@ kvc_status kvc_block_prefill_step(kvc_block_state* st, const void* Kblk, const v
       cp.posd[0] = st->pos[0];
       cp.src_ld = st->capacity;
       cp.dst_ld = st->capacity;
+      cp.Vblk = Vblk;
+      cp.blk_len = blk_len;
+      for (int l = 0; l < L; ++l) cp.blk_row0[l] = st->len[l];
       if (launch_evict_in_place(w.score, ep, w.kept, kmax, cp, cst) != cudaSuccess) return KVC_ERR_CUDA;
     }
     // two slabs: eviction and compaction in one launch; each active layer's

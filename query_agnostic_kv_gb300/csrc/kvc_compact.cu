@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(THREADS) append_kernel(const uint4* __restrict
     const int64_t src = (lh * P.B + t) * 16 + sub;
     const int64_t dst = (lh * P.ld + P.len[l] + t);
     K[dst * 16 + sub] = __ldg(Kb + src);
-    V[dst * 16 + sub] = __ldg(Vb + src);
+    if (t < P.vrows[l]) V[dst * 16 + sub] = __ldg(Vb + src);
     if (sub == 0) pos[dst] = static_cast<int32_t>(P.pos0 + t);
   }
 }

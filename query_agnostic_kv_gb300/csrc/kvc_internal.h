@@ -149,6 +149,12 @@ struct EvictCopy {
   int64_t src_ld;                 // rows per (l, h) in a source slab
   int64_t dst_ld;                 // rows per (l, h) in a destination; < 0: ragged at out_off[l] + h*k_l
   int32_t slab[kMaxLayers];
+  // in-place eviction: when Vblk is set, a moved row r takes its V row from
+  // the block, Vblk[l][h][r - blk_row0[l]] with blk_len rows per (l, h)
+  // (the block's V rows at or above the budget were not appended)
+  const void* Vblk;
+  int32_t blk_len;
+  int32_t blk_row0[kMaxLayers];
 };
 // gmax_word: two zeroed words of device memory when pin is set (the max
 // order key, an arrival counter).  copy: null, or the fused compaction.
@@ -195,6 +201,7 @@ struct AppendParams {
   int64_t ld;                     // rows per (l, h) in the state slab
   int32_t len[kMaxLayers];
   int32_t cur[kMaxLayers];        // which of the two slabs holds layer l
+  int32_t vrows[kMaxLayers];      // V of the block's rows t < vrows[l] is appended (K always is)
   int64_t pos0;                   // global position of the block's first token
 };
 cudaError_t launch_append(const void* Kblk, const void* Vblk, void* K0, void* V0, int32_t* pos0, void* K1, void* V1,

@@ -269,12 +269,16 @@ __device__ void copy_rows(const EvictParams& P, const EvictCopy& X, int l, int h
 // budget and movers at or above it, so no row is both read and written.
 // K and V rows form one stream of 256-byte row copies, half a warp per row,
 // eight in flight per half-warp.
-__device__ void move_rows(const EvictCopy& X, int64_t lh, const int32_t* holes, const int32_t* movers, int p0,
-                          int p1) {
+__device__ void move_rows(const EvictCopy& X, int l, int64_t lh, const int32_t* holes, const int32_t* movers,
+                          int p0, int p1) {
   uint4* K = static_cast<uint4*>(X.Kd[0]);
   uint4* V = static_cast<uint4*>(X.Vd[0]);
   int32_t* pos = X.posd[0];
   const int64_t base = lh * X.src_ld;
+  // V rows of movers come from the block when it is given (row r is block
+  // row r - blk_row0[l])
+  const uint4* Vsrc = X.Vblk ? static_cast<const uint4*>(X.Vblk) : V;
+  const int64_t vbase = X.Vblk ? lh * X.blk_len - X.blk_row0[l] : base;
   const int sub = threadIdx.x & 15, hw = threadIdx.x >> 4;
   constexpr int HW = CT / 16;
   constexpr int R = 8;
@@ -289,7 +293,7 @@ __device__ void move_rows(const EvictCopy& X, int64_t lh, const int32_t* holes, 
       src[u] = -1;
       if (w < total) {
         src[u] = movers[p0 + (w < np ? w : w - np)];
-        val[u] = (w < np ? K : V)[(base + src[u]) * 16 + sub];
+        val[u] = w < np ? K[(base + src[u]) * 16 + sub] : Vsrc[(vbase + src[u]) * 16 + sub];
       }
     }
 #pragma unroll
@@ -412,7 +416,7 @@ __device__ void evict_in_place(cg::cluster_group& cl, TopkShared& sm, uint32_t* 
   const int np = static_cast<int>(sm.sel_cta);
   const int per = (np + C - 1) / C;
   const int p0 = min(rank * per, np), p1 = min(p0 + per, np);
-  move_rows(X, lh, holes, movers, p0, p1);
+  move_rows(X, R.l, lh, holes, movers, p0, p1);
 }
 
 // INPLACE: the in-place eviction (mode 2) only; a separate instance keeps

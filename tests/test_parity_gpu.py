@@ -425,6 +425,11 @@ EPI_CASES = {
     # 20 x 8 over-budget heads at the last blocks: 160 row-LSE units of
     # different lengths on 152 SMs, so the second, reversed wave is taken
     "epi-20x8": dict(L=20, Hkv=8, Hq=24, mean_budget=600),
+    # rows of up to 38K keys: eviction clusters of three CTAs
+    "epi-wide-rows": dict(L=2, Hkv=2, Hq=4, mean_budget=28000, n_hist=70000, block=8192),
+    # 140K history positions: the ordered pack of the one-slab state takes
+    # two bitmap windows of 2^17 positions
+    "epi-long-history": dict(L=2, Hkv=2, Hq=4, mean_budget=700, n_hist=140000, block=8192),
 }
 
 
