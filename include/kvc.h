@@ -306,7 +306,8 @@ KVC_API kvc_status kvc_evict_compact(kvc_shape shape, float* score, int32_t sink
  * reconstruction scoring (each round's mean score replacing the proxy),
  * then eviction and compaction.  Outputs as in the entry points above;
  * p_opt [N], sel_opt [Q] (last pass) and score_opt [L][Hkv][N] may be NULL
- * (the workspace holds them then). */
+ * (the workspace holds them then; without score_opt the sinks' scores are
+ * not pinned, as nothing reads them: the sinks are kept either way). */
 KVC_API kvc_status kvc_compress(kvc_shape shape, const void* K, const void* V, const void* Qpool, int32_t sinks, int32_t m,
                         double rho, int32_t passes, const int32_t* k_per_layer, int32_t* kept, void* Kc, void* Vc,
                         float* p_opt, int32_t* sel_opt, float* score_opt, void* ws, size_t ws_bytes,

@@ -390,7 +390,7 @@ kvc_status run_recon(const kvc_shape& s, const ChunkPlan& plan, int32_t sinks, c
 }
 
 kvc_status run_evict(const kvc_shape& s, float* score, int32_t sinks, const int32_t* k_per_layer, int32_t* kept,
-                     uint32_t* gmax, cudaStream_t st, const EvictCopy* copy = nullptr) {
+                     uint32_t* gmax, cudaStream_t st, const EvictCopy* copy = nullptr, bool pin = true) {
   EvictParams ep;
   memset(&ep, 0, sizeof(ep));
   ep.L = s.L;
@@ -405,7 +405,7 @@ kvc_status run_evict(const kvc_shape& s, float* score, int32_t sinks, const int3
     ep.active[l] = 1;
     off += static_cast<int64_t>(s.Hkv) * k_per_layer[l];
   }
-  return cuda_status(launch_evict(score, ep, kept, gmax, true, copy, st));
+  return cuda_status(launch_evict(score, ep, kept, gmax, pin, copy, st));
 }
 
 kvc_status run_compact(const kvc_shape& s, const void* K, const void* V, const int32_t* kept,
@@ -809,7 +809,9 @@ kvc_status kvc_compress_ex(kvc_shape shape, kvc_proxy_kind proxy, const void* K,
   cp.Vd[0] = Vc;
   cp.src_ld = shape.N;
   cp.dst_ld = -1;
-  return run_evict(shape, score, sinks, k_per_layer, kept, w.gmax, st, &cp);
+  // the sinks are kept by construction; their pinned score is written only
+  // where the caller can read it
+  return run_evict(shape, score, sinks, k_per_layer, kept, w.gmax, st, &cp, score_opt != nullptr);
 }
 
 kvc_status kvc_layer_budgets(const float* sens, int32_t L, double alpha, int64_t mean_budget, int32_t sinks,
