@@ -430,6 +430,10 @@ EPI_CASES = {
     # 140K history positions: the ordered pack of the one-slab state takes
     # two bitmap windows of 2^17 positions
     "epi-long-history": dict(L=2, Hkv=2, Hq=4, mean_budget=700, n_hist=140000, block=8192),
+    # no sinks, blocks of 17 tokens, budgets down to a few rows
+    "epi-no-sinks": dict(L=3, Hkv=2, Hq=4, mean_budget=40, n_hist=400, block=17, sinks=0),
+    # one-token blocks: every step after the budget evicts exactly one row
+    "epi-one-token": dict(L=2, Hkv=1, Hq=2, mean_budget=12, n_hist=60, block=1),
 }
 
 
@@ -487,9 +491,9 @@ def test_block_prefill_matches_oracle(qk, name, layout):
     threshold, the kept K and V rows bit for bit; an under-budget step must
     append the block unchanged.  The one-slab layout holds the same rows in
     another order; its packed image must be in position order."""
-    case = dict(n_hist=1500, block=256)
+    case = dict(n_hist=1500, block=256, sinks=4)
     case.update(EPI_CASES[name])
-    cfg = ks.EpiConfig(name, d=128, episodes=1, prompt_len=24, alpha=3.0, sinks=4, **case)
+    cfg = ks.EpiConfig(name, d=128, episodes=1, prompt_len=24, alpha=3.0, **case)
     sens = ks.gen_sensitivity(cfg)
     budgets = qk.kvc_layer_budgets(sens.tolist(), cfg.alpha, cfg.mean_budget, cfg.sinks)
     assert budgets == kv2.layer_budgets(sens.astype(np.float64), cfg.alpha, cfg.mean_budget, cfg.sinks).tolist()
