@@ -1236,9 +1236,11 @@ def epi_in_place_bytes(qk, cfg, budgets, new_state, blocks, prompt, ws, stream, 
     return total
 
 
-# DRAM bytes (read + write) per eviction + compaction launch of the EpiCache
-# block step, from ncu; None until captured for the fused kernel.
-EPI_EVICT_TRAFFIC_PER_LAUNCH = None
+# DRAM bytes (read + write) per launch of the EpiCache block step's in-place
+# eviction (one-slab state), from a one-pass ncu capture of one episode's 44
+# launches: 52.21 + 8.71 MB on average.  Reset to None whenever the kernel
+# changes until it is captured again.
+EPI_EVICT_TRAFFIC_PER_LAUNCH = (52.21e6 + 8.71e6)
 
 
 def run_epicache(args, rank, world, local_rank):
@@ -1370,8 +1372,9 @@ def run_epicache(args, rank, world, local_rank):
     ach = cbytes / ctime / 1e9
     roof = {"kernel": " + ".join(parts) + f" ({what})", "bound": "hbm",
             "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-            "traffic": EPI_EVICT_TRAFFIC_PER_LAUNCH,
-            "traffic_source": "ncu dram bytes per step (null: not captured for these kernels)",
+            "traffic": EPI_EVICT_TRAFFIC_PER_LAUNCH if n_slab == 1 else None,
+            "traffic_source": "ncu dram bytes per launch, mean over one episode (one-slab layout; null for the "
+                              "two-slab kernels, not captured)",
             "peak_source": f"hbm_gbs of {peak_src} peaks",
             "algorithmic_bytes_per_step": cbytes / steps_scored}
 

@@ -23,7 +23,12 @@
 //      counts (the cluster's counts exchanged once);
 //   4. eviction only: the kept K/V rows are copied into the compacted cache
 //      in the same kernel (optional), and the last CTA to finish pins the
-//      sinks to the global max score.
+//      sinks to the global max score (when the caller reads the scores).
+// A third use, EpiCache's block step ("[26'ICML] EpiCache", "방법: 3단계"
+// step ②) on a one-slab state, evicts in place (a separate instance,
+// INPLACE): instead of the ordered emit, the evicted rows below the budget
+// and the kept rows at or above it are listed and the latter moved into the
+// former; ties at the threshold are ranked by the rows' global positions.
 // Rows longer than kMaxParts shared-memory parts use the global-memory radix
 // kernels at the end of this file.
 #include <cooperative_groups.h>
