@@ -101,13 +101,13 @@ def algorithmic_work(cfg):
 
 
 # DRAM bytes per launch of the row-LSE kernel as ncu counted them (one pass,
-# no replay) on the 4-layer case of the 16K workload, the mean of two
-# launches: dram__bytes_read + dram__bytes_write = 202.59 + 5.69 MB (the
-# writes are the 32-byte lse rows the column-max pass reads, part of them
-# still in L2 when the kernel ends); the traffic grows with the number of
-# (layer, KV head) pairs.  Reset to None whenever the kernel changes until it
-# is captured again.
-LSE_TRAFFIC_PER_LAYER = (202.59e6 + 5.69e6) / 4
+# no replay) on the 4-layer case of the 16K workload, the mean of three
+# launches in two captures: dram__bytes_read + dram__bytes_write = 202.58 +
+# 6.12 MB (the writes are the 32-byte lse rows the column-max pass reads,
+# part of them still in L2 when the kernel ends); the traffic grows with the
+# number of (layer, KV head) pairs.  Reset to None whenever the kernel
+# changes until it is captured again.
+LSE_TRAFFIC_PER_LAYER = (202.58e6 + 6.12e6) / 4
 
 
 def load_peaks():

@@ -137,7 +137,6 @@ struct KParams {
   int32_t ldApp;                      // appended-key rows per (l, h)
   int32_t units1;                     // pass-1 units per (l, h)
   int32_t snake;                      // pass 1: odd waves in reverse CTA order
-  int32_t early_b;                    // pass 2: per-tile A barriers, each unit's first B tile ahead of its A tiles
   int n_units;
   float scale_log2;                   // log2(e) / sqrt(d)
   __nv_bfloat16* lsx;                 // [rows][16]: -lse2/scale_log2 in three bf16 terms
@@ -384,7 +383,9 @@ __device__ __forceinline__ void lse_update_lazy(float (&v)[N], int lim, float c,
 }
 
 
-template <int PASS>
+// EARLY (pass 2 only): units of at most two query tiles, whose first query
+// tile is issued ahead of their key tiles, with a barrier pair per key tile.
+template <int PASS, bool EARLY = false>
 __global__ void __launch_bounds__(kThreads<PASS>, 1)
     recon_kernel(const __grid_constant__ CUtensorMap tmQg, const __grid_constant__ CUtensorMap tmK0,
                  const __grid_constant__ CUtensorMap tmK1, const __grid_constant__ CUtensorMap tmApp,
@@ -394,6 +395,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
   constexpr int BSTAGE = kBStage<PASS>;            // bytes of one B tile
   constexpr int BHALF = BSTAGE / 2;                // one 64-column swizzled half of a B tile
   constexpr int AHALF = TILE_BYTES / 2;
+  constexpr bool kEarly = PASS == 2 && EARLY;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;                              // [ABUF][NA] tiles
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    static_assert(ABUF <= 2 && (PASS == 1 || (ABUF == 1 && NA <= 2)), "A barriers");
+    static_assert(ABUF <= 2 && (!kEarly || (ABUF == 1 && NA <= 2)), "A barriers");
     for (int i = 0; i < 2; ++i) {      // pass 1: per A buffer; pass 2: per A tile
       mbar_init(&bars->a_full[i], 1);
       mbar_init(&bars->a_empty[i], 1);
@@ -468,78 +470,83 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
         y = static_cast<int32_t>(W.lh * P.ldK + W.key0 + t * TILE_ROWS);
         return W.slab ? &tmK1 : &tmK0;
       };
-      for (int k = 0, u; (u = unit_of_wave<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
-        const Unit U = decode_unit<PASS>(P, u);
-        auto prefetch_next = [&]() {
-          const int un = unit_of_wave<PASS>(P, k + 1);
-          if (un < 0) return;
-          const Unit W = decode_unit<PASS>(P, un);
-          for (int t = 0; t < W.ntile; ++t) {
-            int32_t y;
-            const CUtensorMap* map = a_tile(W, t, y);
-            tma_prefetch_l2_2d(map, 0, y);
-            tma_prefetch_l2_2d(map, 64, y);
-          }
-        };
-        // B tile i (BN rows)
-        auto issue_b = [&](int i) -> bool {
-          if (*abort_flag) return false;
-          if (!mbar_wait(&bars->b_empty[s], bph ^ 1, P.limit_ns)) { fail(); return false; }
-          mbar_arrive_expect_tx(&bars->b_full[s], BSTAGE + BX_STAGE);
-          const CUtensorMap* map;
-          int32_t y;
-          if (PASS == 1) {
-            const TileRef tr = tile_at1(P, U, i);
-            if (tr.kind == 0) {
-              map = U.slab ? &tmK1 : &tmK0;
-              y = static_cast<int32_t>(U.lh * P.ldK + tr.t0);
-            } else {
-              map = &tmApp;
-              y = U.lh * P.ldApp + tr.chunk * P.nq_full + tr.t0;
-            }
-          } else {
-            map = &tmQg;
-            y = U.lh * P.Rpad + U.r * P.CR + i * BN;
-            // pass 2 receives the lse-row map in the appended-key slot
-            tma_load_2d(sBx + s * BX_STAGE, &tmApp, 0, y, &bars->b_full[s]);
-          }
-          uint8_t* dst = sB + s * BSTAGE;
-          tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
-          tma_load_2d(dst + BHALF, map, 64, y, &bars->b_full[s]);
-          ++loads_b;
-          if (PASS == 2 && i == min(1, U.nT - 1)) prefetch_next();
-          if (++s == KST) { s = 0; bph ^= 1; }
-          return true;
-        };
-        int b_from = 0;
-        if (PASS == 2 && P.early_b) {
-          // Units of one or two query tiles (short prompts): the unit's first
-          // query tile goes out before its key tiles, so it loads while the
-          // previous unit's MMAs still hold the A buffer, and each key tile
-          // has its own barrier pair and is refilled as soon as the previous
-          // unit's last MMA on it is done (EpiCache's one-tile prompts: 0.157
-          // -> 0.134 ms per step).  Units of many query tiles keep one
-          // barrier pair for the buffer: there the reloads are rare, and the
-          // split barriers measured 0.8% slower at 32 layers of the 16K
-          // workload.
-          if (!issue_b(0)) break;
-          b_from = 1;
-          bool ok = true;
-          for (int t = 0; t < NA; ++t) {
-            if (!mbar_wait(&bars->a_empty[t], aph ^ 1, P.limit_ns)) { fail(); ok = false; break; }
-            if (t < U.ntile) {
-              mbar_arrive_expect_tx(&bars->a_full[t], TILE_BYTES);
-              uint8_t* dst = sA + t * TILE_BYTES;
+      if constexpr (kEarly) {
+        for (int k = 0, u; (u = unit_of_wave<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
+          const Unit U = decode_unit<PASS>(P, u);
+          auto prefetch_next = [&]() {
+            const int un = unit_of_wave<PASS>(P, k + 1);
+            if (un < 0) return;
+            const Unit W = decode_unit<PASS>(P, un);
+            for (int t = 0; t < W.ntile; ++t) {
               int32_t y;
-              const CUtensorMap* map = a_tile(U, t, y);
-              tma_load_2d(dst, map, 0, y, &bars->a_full[t]);
-              tma_load_2d(dst + AHALF, map, 64, y, &bars->a_full[t]);
-            } else {
-              mbar_arrive(&bars->a_full[t]);    // a missing tile completes its phase empty
+              const CUtensorMap* map = a_tile(W, t, y);
+              tma_prefetch_l2_2d(map, 0, y);
+              tma_prefetch_l2_2d(map, 64, y);
             }
+          };
+          // B tile i (BN rows)
+          auto issue_b = [&](int i) -> bool {
+            if (*abort_flag) return false;
+            if (!mbar_wait(&bars->b_empty[s], bph ^ 1, P.limit_ns)) { fail(); return false; }
+            mbar_arrive_expect_tx(&bars->b_full[s], BSTAGE + BX_STAGE);
+            const CUtensorMap* map;
+            int32_t y;
+            if (PASS == 1) {
+              const TileRef tr = tile_at1(P, U, i);
+              if (tr.kind == 0) {
+                map = U.slab ? &tmK1 : &tmK0;
+                y = static_cast<int32_t>(U.lh * P.ldK + tr.t0);
+              } else {
+                map = &tmApp;
+                y = U.lh * P.ldApp + tr.chunk * P.nq_full + tr.t0;
+              }
+            } else {
+              map = &tmQg;
+              y = U.lh * P.Rpad + U.r * P.CR + i * BN;
+              // pass 2 receives the lse-row map in the appended-key slot
+              tma_load_2d(sBx + s * BX_STAGE, &tmApp, 0, y, &bars->b_full[s]);
+            }
+            uint8_t* dst = sB + s * BSTAGE;
+            tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
+            tma_load_2d(dst + BHALF, map, 64, y, &bars->b_full[s]);
+            ++loads_b;
+            if (PASS == 2 && i == min(1, U.nT - 1)) prefetch_next();
+            if (++s == KST) { s = 0; bph ^= 1; }
+            return true;
+          };
+          // The unit's first query tile goes out before its key tiles, so it
+          // loads while the previous unit's MMAs still hold the A buffer, and
+          // each key tile has its own barrier pair and is refilled as soon as
+          // the previous unit's last MMA on it is done (EpiCache's one-tile
+          // prompts: 0.157 -> 0.134 ms per step).  Units of many query tiles
+          // use the buffer-wide loop below: there the reloads are rare, and
+          // this one measured 3-7% slower at 32 layers of the 16K workload.
+          {
+            if (!issue_b(0)) break;
+            bool ok = true;
+            for (int t = 0; t < NA; ++t) {
+              if (!mbar_wait(&bars->a_empty[t], aph ^ 1, P.limit_ns)) { fail(); ok = false; break; }
+              if (t < U.ntile) {
+                mbar_arrive_expect_tx(&bars->a_full[t], TILE_BYTES);
+                uint8_t* dst = sA + t * TILE_BYTES;
+                int32_t y;
+                const CUtensorMap* map = a_tile(U, t, y);
+                tma_load_2d(dst, map, 0, y, &bars->a_full[t]);
+                tma_load_2d(dst + AHALF, map, 64, y, &bars->a_full[t]);
+              } else {
+                mbar_arrive(&bars->a_full[t]);    // a missing tile completes its phase empty
+              }
+            }
+            if (!ok) break;
           }
-          if (!ok) break;
-        } else {
+          ++loads_a;
+          if (++ab == ABUF) { ab = 0; aph ^= 1; }
+          for (int i = 1; i < U.nT; ++i)
+            if (!issue_b(i)) break;
+        }
+      } else {
+        for (int k = 0, u; (u = unit_of_wave<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
+          const Unit U = decode_unit<PASS>(P, u);
           if (!mbar_wait(&bars->a_empty[ab], aph ^ 1, P.limit_ns)) { fail(); break; }
           mbar_arrive_expect_tx(&bars->a_full[ab], U.ntile * TILE_BYTES);
           for (int t = 0; t < U.ntile; ++t) {
@@ -549,16 +556,54 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
             tma_load_2d(dst, map, 0, y, &bars->a_full[ab]);
             tma_load_2d(dst + AHALF, map, 64, y, &bars->a_full[ab]);
           }
+          ++loads_a;
+          auto prefetch_next = [&]() {
+            const int un = unit_of_wave<PASS>(P, k + 1);
+            if (un < 0) return;
+            const Unit W = decode_unit<PASS>(P, un);
+            for (int t = 0; t < W.ntile; ++t) {
+              int32_t y;
+              const CUtensorMap* map = a_tile(W, t, y);
+              tma_prefetch_l2_2d(map, 0, y);
+              tma_prefetch_l2_2d(map, 64, y);
+            }
+          };
+          if (++ab == ABUF) { ab = 0; aph ^= 1; }
+          // B tiles (BN rows each)
+          for (int i = 0; i < U.nT; ++i) {
+            if (*abort_flag) break;
+            if (!mbar_wait(&bars->b_empty[s], bph ^ 1, P.limit_ns)) { fail(); break; }
+            mbar_arrive_expect_tx(&bars->b_full[s], BSTAGE + BX_STAGE);
+            const CUtensorMap* map;
+            int32_t y;
+            if (PASS == 1) {
+              const TileRef tr = tile_at1(P, U, i);
+              if (tr.kind == 0) {
+                map = U.slab ? &tmK1 : &tmK0;
+                y = static_cast<int32_t>(U.lh * P.ldK + tr.t0);
+              } else {
+                map = &tmApp;
+                y = U.lh * P.ldApp + tr.chunk * P.nq_full + tr.t0;
+              }
+            } else {
+              map = &tmQg;
+              y = U.lh * P.Rpad + U.r * P.CR + i * BN;
+              // pass 2 receives the lse-row map in the appended-key slot
+              tma_load_2d(sBx + s * BX_STAGE, &tmApp, 0, y, &bars->b_full[s]);
+            }
+            uint8_t* dst = sB + s * BSTAGE;
+            tma_load_2d(dst, map, 0, y, &bars->b_full[s]);
+            tma_load_2d(dst + BHALF, map, 64, y, &bars->b_full[s]);
+            ++loads_b;
+            if (PASS == 2 && i == min(1, U.nT - 1)) prefetch_next();
+            if (++s == KST) { s = 0; bph ^= 1; }
+          }
         }
-        ++loads_a;
-        if (++ab == ABUF) { ab = 0; aph ^= 1; }
-        for (int i = b_from; i < U.nT; ++i)
-          if (!issue_b(i)) break;
       }
       // Wait for every copy this thread started (normally already consumed).
       for (int i = 0; i < KST; ++i)
         if (loads_b > i) mbar_wait(&bars->b_full[i], ((loads_b - 1 - i) / KST) & 1, P.limit_ns);
-      if (PASS == 2 && P.early_b) {
+      if constexpr (kEarly) {
         for (int t = 0; t < NA; ++t)
           if (loads_a > 0) mbar_wait(&bars->a_full[t], (loads_a - 1) & 1, P.limit_ns);
       } else {
@@ -574,7 +619,7 @@ __global__ void __launch_bounds__(kThreads<PASS>, 1)
       uint32_t bph = 0, aph = 0, dph = 0;
       for (int k = 0, u; (u = unit_of_wave<PASS>(P, k)) >= 0 && !*abort_flag; ++k) {
         const Unit U = decode_unit<PASS>(P, u);
-        const bool per_tile = PASS == 2 && P.early_b;
+        constexpr bool per_tile = kEarly;
         if (!per_tile) {
           if (!mbar_wait(&bars->a_full[ab], aph, P.limit_ns)) { fail(); break; }
           tc_fence_after();
@@ -1005,7 +1050,7 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   for (int a = 1; a < pr.n_active; ++a)
     if (pr.lay[a].n != pr.lay[0].n) kp.snake = 1;
   // pass-2 units of at most two query tiles: early B tiles, per-tile A barriers
-  kp.early_b = (static_cast<int64_t>(G) * std::max(pr.nq_full, pr.nq_last) <= 2 * Cfg<2>::BN) ? 1 : 0;
+  const bool early2 = static_cast<int64_t>(G) * std::max(pr.nq_full, pr.nq_last) <= 2 * Cfg<2>::BN;
   kp.ldK = pr.ldK;
   kp.nq_full = pr.nq_full; kp.nq_last = pr.nq_last; kp.Q = pr.Q;
   kp.CR = CR; kp.Rpad = Rpad;
@@ -1023,6 +1068,8 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   if (ea != cudaSuccess) return ea;
   ea = cudaFuncSetAttribute(recon_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes<2>);
   if (ea != cudaSuccess) return ea;
+  ea = cudaFuncSetAttribute(recon_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes<2>);
+  if (ea != cudaSuccess) return ea;
   const int sms = num_sms();
   // pass 1
   kp.n_units = pr.n_active * pr.Hkv * kp.units1;
@@ -1037,8 +1084,11 @@ cudaError_t launch_recon(const ReconProblem& pr, const ReconWorkspace& ws, cudaS
   kp.n_units = acc;
   if ((phases & RECON_COLS) && kp.n_units > 0) {
     ProfScope ps("recon_colmax", st);
-    recon_kernel<2><<<kp.n_units < sms ? kp.n_units : sms, kThreads<2>, kSmemBytes<2>, st>>>(tmQgB, tmK0a, tmK1a,
-                                                                                            tmLx, kp);
+    const unsigned grid2 = kp.n_units < sms ? kp.n_units : sms;
+    if (early2)
+      recon_kernel<2, true><<<grid2, kThreads<2>, kSmemBytes<2>, st>>>(tmQgB, tmK0a, tmK1a, tmLx, kp);
+    else
+      recon_kernel<2><<<grid2, kThreads<2>, kSmemBytes<2>, st>>>(tmQgB, tmK0a, tmK1a, tmLx, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
