@@ -722,3 +722,27 @@ def test_compress_in_cuda_graph(qk):
         torch.cuda.synchronize()
         assert qk.kvc_stream_status() == 0
         assert torch.equal(kept, ref[0]) and torch.equal(Kc, ref[1]) and torch.equal(Vc, ref[2])
+
+
+def test_block_state_init_validation(qk):
+    """The one-slab layout needs all three second-slab buffers absent and a
+    capacity its eviction kernel covers; mixed or oversized states are refused
+    on the host (KVC_ERR_INVALID) before any device work."""
+    L, H, Hq, S = 2, 2, 4, 4
+    small = [torch.zeros(L * H * 64 * 128, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
+    pos = [torch.zeros(L * H * 64, dtype=torch.int32, device=DEV) for _ in range(2)]
+    st = qk.kvc_block_state_init(L, H, Hq, 64, S, [16, 32], small[0], small[1], pos[0])
+    assert st.K[1] is None and st.cur[0] == 0
+    with pytest.raises(qk.KVCError):      # a second K slab without its V and positions
+        qk.kvc_block_state_init(L, H, Hq, 64, S, [16, 32], small[0], small[1], pos[0], small[2], None, None)
+    with pytest.raises(qk.KVCError):      # a budget above the capacity
+        qk.kvc_block_state_init(L, H, Hq, 64, S, [16, 65], small[0], small[1], pos[0])
+    big = 393216 + 128                    # more rows than the in-place eviction covers
+    kb = torch.zeros(1 * 1 * big * 128, dtype=torch.bfloat16, device=DEV)
+    vb = torch.zeros_like(kb)
+    pb = torch.zeros(big, dtype=torch.int32, device=DEV)
+    with pytest.raises(qk.KVCError):
+        qk.kvc_block_state_init(1, 1, 2, big, S, [1000], kb, vb, pb)
+    # the same capacity is fine with two slabs (their eviction falls back to the global-memory kernels)
+    kb2, vb2, pb2 = torch.zeros_like(kb), torch.zeros_like(vb), torch.zeros_like(pb)
+    qk.kvc_block_state_init(1, 1, 2, big, S, [1000], kb, vb, pb, kb2, vb2, pb2)
