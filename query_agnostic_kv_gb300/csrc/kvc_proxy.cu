@@ -104,10 +104,11 @@ __device__ __forceinline__ float transpose_sum8(const float (&v)[8], int l16) {
   return r3 + __shfl_xor_sync(0xffffffffu, r3, 1);
 }
 
-// Pass B reads each row for the last time: its loads carry an L2
-// evict-first policy, so the rows it has consumed leave L2 before the rows
-// other heads' pass B still needs (16K workload: 0.303 -> 0.289 ms; an
-// evict-last policy on pass A's loads changed nothing).
+// Loads of rows that L2 will not serve again carry an L2 evict-first
+// policy, so they leave L2 before the rows other heads' pass B still needs:
+// every load of pass B (each row's last read), and pass A's loads of the
+// rows kept in shared memory for pass B (16K workload: 0.303 -> 0.289 ->
+// 0.280 ms; an evict-last policy on pass A's other loads changed nothing).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -146,6 +147,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
   const int u_own = l16 >> 1;                 // row (of the eight) this lane ends up owning
   const bool writer = (l16 & 1) == 0;
 
+  const uint64_t cached_read = l2_policy_evict_first();
   // ---- pass A: sum of unit keys over the slice; 1/|k_i| kept in s[i]
   uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
   for (int base = i0; base < i1; base += HALVES * UNROLL) {
@@ -153,7 +155,10 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, CTAS_
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int i = base + u * HALVES + hw;
-      q[u] = (i < i1) ? __ldg(rows + static_cast<int64_t>(i) * 16 + l16) : make_uint4(0, 0, 0, 0);
+      // rows that pass B reads from the shared-memory copy are not needed in L2 again
+      q[u] = (i < i1) ? ((i - i0 < CACHE_ROWS) ? ld_nc_policy(rows + static_cast<int64_t>(i) * 16 + l16, cached_read)
+                                             : __ldg(rows + static_cast<int64_t>(i) * 16 + l16))
+                      : make_uint4(0, 0, 0, 0);
     }
     if (KD_PREFETCH) {
       // warm L2 with the rows KD_PREFETCH steps ahead: lane l16 takes line (l16 & 1) of row (l16 >> 1)
