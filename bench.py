@@ -1303,6 +1303,8 @@ def run_epicache(args, rank, world, local_rank):
                Vblk[b] if b < nb - 1 or cfg.n_hist % B == 0 else Vblk[b, :, :, :cfg.n_hist - b * B].contiguous(),
                min(B, cfg.n_hist - b * B)) for b in range(nb)]
 
+    last_state = []
+
     def episode(e, ws=None):
         st = new_state()
         if ws is None:
@@ -1310,6 +1312,7 @@ def run_epicache(args, rank, world, local_rank):
         dq, dk = prompts[e]
         for kb, vb, n in blocks:
             qk.kvc_block_prefill_step(st, kb, vb, n, dq, dk, P, ws=ws, stream=stream)
+        last_state[:] = [st]
         return ws
 
     n_warm = max(3, args.warmup)
@@ -1378,6 +1381,33 @@ def run_epicache(args, rank, world, local_rank):
             "peak_source": f"hbm_gbs of {peak_src} peaks",
             "algorithmic_bytes_per_step": cbytes / steps_scored}
 
+    # the episode's packed image (kvc_episode_pack): one contiguous copy of the
+    # kept rows in ascending position order per (layer, KV head); for the
+    # one-slab state this is where the position order is restored
+    st_last = last_state[0]
+    R = qk.kvc_episode_rows(st_last)
+    Kp = torch.empty(R * 128, dtype=torch.bfloat16, device=dev)
+    Vp = torch.empty_like(Kp)
+    Pp = torch.empty(R, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        qk.kvc_episode_pack(st_last, Kp, Vp, Pp, stream=stream)
+    torch.cuda.synchronize()
+    pa = torch.cuda.Event(enable_timing=True)
+    pb = torch.cuda.Event(enable_timing=True)
+    pa.record(stream)
+    for _ in range(20):
+        qk.kvc_episode_pack(st_last, Kp, Vp, Pp, stream=stream)
+    pb.record(stream)
+    torch.cuda.synchronize()
+    assert qk.kvc_stream_status() == 0
+    pack_ms = pa.elapsed_time(pb) / 20
+    pack_bytes = R * (2 * 2 * 128 * 2 + 2 * 4)      # K and V rows read and written, positions
+    pack = {"ms": pack_ms, "rows": R, "GB/s": pack_bytes / (pack_ms / 1e3) / 1e9,
+            "frac_of_hbm": pack_bytes / (pack_ms / 1e3) / 1e9 / hbm if hbm else None,
+            "ordered": n_slab == 1,
+            "how": "kvc_episode_pack of the last timed episode's state, 20 back-to-back calls (CUDA events); algorithmic "
+                   "bytes = every kept K and V row read and written plus its position"}
+
     # end to end: the history streamed from pinned host memory; block b is
     # copied on a copy stream into one of two device buffers while the step
     # of block b - 1 runs
@@ -1441,7 +1471,7 @@ def run_epicache(args, rank, world, local_rank):
                    "n_hist": cfg.n_hist, "block": B, "episodes": cfg.episodes, "prompt_queries": P, "mean_budget": cfg.mean_budget, "alpha": cfg.alpha,
                    "step": "one episode (all history blocks)", "l2": "history 10 GB on the device"},
         "roofline": roof, "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()), "clocks": clocks,
-        "memory": memory, "e2e": e2e, "cpu_baseline": cpu}), flush=True)
+        "memory": memory, "pack": pack, "e2e": e2e, "cpu_baseline": cpu}), flush=True)
 
 
 # ---------------------------------------------------------------- reconstruction-ratio sweep
