@@ -355,8 +355,8 @@ typedef struct {
   int32_t L, Hkv, Hq, d;
   int32_t capacity;               /* rows per (layer, KV head) in each slab: >= max budget + block */
   int32_t sinks;
-  void* K[2];                     /* device bf16 [L][Hkv][capacity][d], two slabs */
-  void* V[2];                     /* device bf16 [L][Hkv][capacity][d], two slabs */
+  void* K[2];                     /* device bf16 [L][Hkv][capacity][d] per slab ([1] NULL: one slab) */
+  void* V[2];                     /* device bf16 [L][Hkv][capacity][d] per slab ([1] NULL: one slab) */
   int32_t* pos[2];                /* device int32 [L][Hkv][capacity]: global position of each row */
   int32_t cur[KVC_MAX_LAYERS];    /* host: slab holding layer l */
   int32_t len[KVC_MAX_LAYERS];    /* host: rows held per layer (same for every KV head) */
